@@ -1,0 +1,404 @@
+"""Benchmark of the WeDLM window decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload full_stack|low_entropy|one_layer]
+
+A step is one pass of the whole hot path (reorder + embed, every decoder
+layer with paged window attention, LM head with streaming softmax, Eq. 11
+selection, commit and refill) over one batch of synthetic input.  The
+default workload is the full 36-layer Qwen3-8B-shaped random-init bf16 stack,
+prefix 4096, W=16, batch 8, streaming from an all-masked window.
+
+Prints ONE JSON line (rank 0).  `value` = committed tokens/s over the timed
+steps (inputs resident in HBM; the 15 GB of weights exceed L2, so no flush
+is needed); `e2e` = the same metric through the Python API with the window
+copied from pinned host memory and the results read back every step.  The
+multi-GPU path runs independent replicas (one process per GPU, no
+collective): `value` sums the tokens all ranks committed over the max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from synth import WORKLOADS, make_state_np, plant_bias_for, plant_targets  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_stack",
+                    choices=["full_stack", "low_entropy", "one_layer"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per launch of each kernel kind (HBM roofline units)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(shape, B, W, prefix_total):
+    s = shape
+    es = 2 if s.dtype == "bf16" else 4
+    M = B * W
+    H, hd, nq, nkv, F, V = s.hidden, s.head_dim, s.n_q_heads, s.n_kv_heads, s.ffn, s.vocab
+    qkv_rows = (nq + 2 * nkv) * hd
+    return {
+        "gemm_qkv": es * (qkv_rows * H + M * H + M * qkv_rows),
+        "gemm_o": es * (H * nq * hd + M * nq * hd + 2 * M * H),
+        "gemm_gateup": es * (2 * F * H + M * H + M * F),
+        "gemm_down": es * (H * F + M * F + 2 * M * H),
+        "lmhead": es * (V * H + M * H),
+        # every cached K/V byte once + window K/V + q in + o out
+        "attn": es * (prefix_total * 2 * nkv * hd + B * W * 2 * nkv * hd + 2 * M * nq * hd),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = [l.split(",") for l in open(self.f.name).read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload set-up on the device
+# ---------------------------------------------------------------------------
+def setup(wl_name, steps, warmup, device):
+    import torch
+    from synth import make_pool_torch, make_weights_torch
+    wl = WORKLOADS[wl_name]
+    s = wl.shape
+    extra = int(math.ceil((steps + warmup + 4) * wl.window / s.page_block)) + 1
+    import dataclasses
+    wl = dataclasses.replace(wl, extra_pages=extra)
+    st = make_state_np(wl)
+    w = make_weights_torch(s, seed=wl.seed, device=device)
+    pools = [make_pool_torch(s, st["num_pages"], wl.seed, l, device=device)
+             for l in range(s.n_layers)]
+    plant = None
+    if wl.plant:
+        plant = plant_targets(st["pos"], s0=17)
+    return wl, st, w, pools, plant
+
+
+def cpu_sample(wl, w, st, ctx_commits_per_step):
+    """Time the oracle (as it stands) on a bounded sample of one step: one
+    decoder layer over one sequence's window, the LM head over 2 rows and
+    the selection of one sequence, scaled to the whole step (all layers, all
+    sequences, all rows)."""
+    import torch
+    import oracle as O
+    s = wl.shape
+    W = wl.window
+    lw = {k: v.float().cpu().numpy() for k, v in w["layers"][0].items()}
+    lm = w["lm_head"].float().cpu().numpy()
+    norm = w["final_norm"].float().cpu().numpy()
+    rng = np.random.default_rng(0)
+    x = O.bf16_round(rng.standard_normal((W, s.hidden)) * 0.05)
+    L = int(st["seq_len"][0])
+    kp = O.bf16_round(rng.standard_normal((L, s.n_kv_heads, s.head_dim)))
+    vp = O.bf16_round(rng.standard_normal((L, s.n_kv_heads, s.head_dim)))
+    cos, sin = O.rope_cos_sin(st["pos"][0], s.head_dim, s.rope_theta)
+    store = O.storer(s.dtype)
+    t0 = time.perf_counter()
+    O.layer_forward(s, lw, x, cos, sin, kp, vp, store)
+    t_layer = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    h = store(O.rmsnorm(x[:2], norm, s.rms_eps))
+    O.softmax_scores(O.lm_head_logits(h, lm, s.mask_id))
+    t_head2 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    H = rng.uniform(10, 12, W)
+    O.select_eq11(H, st["pos"][0], st["obs"][0], wl.alpha, wl.tau)
+    O.commit_run(st["obs"][0], st["pos"][0], L)
+    t_sel = time.perf_counter() - t0
+    B = wl.batch
+    t_step = B * (s.n_layers * t_layer + (W / 2.0) * t_head2 + t_sel)
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) or cores
+    except Exception:
+        pass
+    return {"value": ctx_commits_per_step / t_step, "unit": "committed tokens/s",
+            "cores": cores, "kind": "oracle",
+            "sample": (f"1 of {s.n_layers} layers x 1 of {B} sequences ({W} rows, prefix {L}), "
+                       f"LM head on 2 of {B * W} rows, selection of 1 sequence; "
+                       f"{t_layer + t_head2 + t_sel:.1f} s measured, scaled to a "
+                       f"{t_step:.1f} s step"),
+            "seconds_per_step": t_step}
+
+
+def run_ours(args):
+    import torch
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    from serving_wedlm_step_gb300.binding import WedlmContext
+    wl, st, w, pools, plant = setup(args.workload, args.steps, args.warmup, device)
+    s = wl.shape
+    B, W = wl.batch, wl.window
+    ctx = WedlmContext(s, w, window=W, max_batch=B, max_pages_per_seq=st["max_pages"])
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    bufs = [{"tokens": T(st["tokens"]), "pos": T(st["pos"]), "obs": T(st["obs"])},
+            {"tokens": T(st["tokens"]), "pos": T(st["pos"]), "obs": T(st["obs"])}]
+    outs = [ctx.make_outputs(B, device=device), ctx.make_outputs(B, device=device)]
+    for i in range(2):  # step i reads bufs[i], writes outs[i] -> copied view of bufs[1-i]
+        outs[i]["new_tokens"] = bufs[1 - i]["tokens"]
+        outs[i]["new_pos"] = bufs[1 - i]["pos"]
+        outs[i]["new_observed"] = bufs[1 - i]["obs"]
+    seq_len = T(st["seq_len"])
+    page_table = T(st["page_table"])
+    plant_t = T(plant) if plant is not None else None
+    bias = plant_bias_for(s.vocab) if plant is not None else 0.0
+    stream = torch.cuda.current_stream(device)
+
+    def one(i):
+        b = bufs[i % 2]
+        ctx.step(b["tokens"], b["pos"], b["obs"], seq_len, page_table, pools, st["num_pages"],
+                 wl.alpha, wl.tau, outs[i % 2], plant_token=plant_t, plant_bias=bias,
+                 stream=stream)
+
+    k = 0
+    for _ in range(args.warmup):
+        one(k)
+        k += 1
+    torch.cuda.synchronize()
+    if ctx.status() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    len0 = int(seq_len.sum())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one(k)
+        k += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    committed = int(seq_len.sum()) - len0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, committed], dtype=torch.float64, device=device)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        ms, committed = float(mx[0]), int(sm[1])
+    if ctx.status() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+    value = committed / (ms / 1e3)
+    prefix_total = int(np.asarray(st["seq_len"]).sum())
+
+    # ---- end to end through the Python API with host buffers -------------
+    e2e_steps = max(4, min(args.steps, 32))
+    # continue the stream from the device state the timed loop left behind
+    last = bufs[k % 2]
+    host = {k2: last[k2].cpu().pin_memory() for k2 in ("tokens", "pos", "obs")}
+    cur = {k2: v.to(device) for k2, v in host.items()}
+    back = {k2: torch.empty_like(host[k2]).pin_memory() for k2 in ("tokens", "pos", "obs")}
+    back_c = torch.empty(B, W, dtype=torch.int32).pin_memory()
+    back_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    out = ctx.make_outputs(B, device=device)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in back.values()) + back_c.numel() * 4 + B * 4
+    n_e2e = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for k2 in cur:
+            cur[k2].copy_(host[k2], non_blocking=True)
+        ctx.step(cur["tokens"], cur["pos"], cur["obs"], seq_len, page_table, pools,
+                 st["num_pages"], wl.alpha, wl.tau, out, plant_token=plant_t, plant_bias=bias,
+                 stream=stream)
+        back["tokens"].copy_(out["new_tokens"], non_blocking=True)
+        back["pos"].copy_(out["new_pos"], non_blocking=True)
+        back["obs"].copy_(out["new_observed"], non_blocking=True)
+        back_c.copy_(out["committed"], non_blocking=True)
+        back_n.copy_(out["n_committed"], non_blocking=True)
+        stream.synchronize()
+        n_e2e += int(back_n.sum())
+        for k2 in host:
+            host[k2].copy_(back[k2])
+    e2e_s = time.perf_counter() - t0
+    e2e_value = n_e2e / e2e_s
+
+    # ---- per-kernel CUDA-event timing (eager launches) --------------------
+    ctx.set_timing(True)
+    n_timing = 8
+    for _ in range(n_timing):
+        one(k)
+        k += 1
+    torch.cuda.synchronize()
+    tim = ctx.timings()
+    ctx.set_timing(False)
+    byts = algorithmic_bytes(s, B, W, int(seq_len.sum()) - B * W)  # lengths mid-run
+    hbm, tf, peak_src = load_peaks()
+    kernels = {}
+    for kind, (kms, n) in tim.items():
+        if n == 0:
+            continue
+        d = {"ms_total": round(kms, 4), "launches": n, "us_per_launch": round(1e3 * kms / n, 2)}
+        if kind in byts:
+            d["gbs"] = round(byts[kind] / (kms / n * 1e-3) / 1e9, 1)
+            d["frac_hbm"] = round(d["gbs"] / hbm, 3)
+        kernels[kind] = d
+    dom = max((k2 for k2 in kernels if k2 in byts), key=lambda k2: kernels[k2]["ms_total"])
+    dk = kernels[dom]
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        traffic = json.load(open(tfile)).get(f"{args.workload}:{dom}")
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm,
+                "unit": "GB/s", "frac": round(dk["gbs"] / hbm, 3), "traffic": traffic,
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": byts[dom]}
+    launches = ctx.launches_per_step(B)
+
+    res = {
+        "metric": "committed tokens/s of the window decode step (step latency in ms_per_step)",
+        "value": round(value, 2), "unit": "committed tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4),
+        "step_latency_us": round(1e3 * ms / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if s.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded random-init weights N(0,0.02), random prefix KV N(0,1))",
+        "config": {"workload": wl.describe(), "global_batch": B * world, "window": W,
+                   "prefix": wl.prefix, "layers": s.n_layers, "alpha": wl.alpha,
+                   "tau": wl.tau, "l2": "inputs larger than L2 (15 GB of weights per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "committed_per_step": round(committed / args.steps / world, 3),
+                   "prefix_cacheability_Pc": round(committed / (args.steps * world * B * W), 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "committed tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": e2e_steps},
+        "gpu_launches": launches * args.steps,
+        "launches_per_step": launches,
+        "clocks": clk,
+        "roofline": roofline,
+        "kernels": kernels,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_sample(wl, w, st, committed / args.steps / world)
+        res["cpu_baseline"].pop("seconds_per_step", None)
+    if rank == 0:
+        print(json.dumps(res))
+    ctx.close()
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, each step a bounded
+    sample of the same workload (see cpu_sample), on rank 0 only."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from synth import make_weights_torch
+    wl = WORKLOADS[args.workload]
+    s = wl.shape
+    st = make_state_np(wl)
+    # the oracle needs one layer + the LM head: draw them on the CPU
+    w = make_weights_torch(s.replace(n_layers=1), seed=wl.seed, device="cpu")
+    commits_per_step = float(wl.batch)  # the all-masked random-init stream commits ~1/seq
+    samples = []
+    t_all = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        r = cpu_sample(wl, w, st, commits_per_step)
+        if i >= args.warmup:
+            samples.append(r["seconds_per_step"])
+        if time.perf_counter() - t_all > 240:
+            break
+    t_step = statistics.median(samples) if samples else r["seconds_per_step"]
+    value = commits_per_step / t_step
+    res = {"impl": "reference",
+           "metric": "committed tokens/s of the window decode step (step latency in ms_per_step)",
+           "value": round(value, 6), "unit": "committed tokens/s", "n_gpus": world,
+           "steps": len(samples), "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic", "config": {"workload": wl.describe()},
+           "cpu_baseline": {"value": round(value, 6), "unit": "committed tokens/s",
+                            "cores": r["cores"], "kind": "oracle", "sample": r["sample"]},
+           "e2e": {"value": round(value, 6), "unit": "committed tokens/s",
+                   "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * wedlm.h — C ABI of libwedlm: one WeDLM window decode step on one GB300.
+ *
+ * The operation is the inference step of "WeDLM: Reconciling Diffusion
+ * Language Models with Standard Causal Attention for Fast Inference"
+ * (bud-325 summary page, Method section; Key claims §3.2, §4.1, §5.2):
+ * reorder the W-slot window so observed tokens come first (RoPE keeps each
+ * token's logical position), run a causal forward of the window on top of
+ * the cached, paged prefix KV, score every masked slot by the entropy of its
+ * softmax, pick slots to fill with the distance-penalised entropy
+ * H~_j = H_j + alpha * d_j (Eq. 11), commit the leftmost contiguous observed
+ * run into the KV cache and refill the freed slots with [M].
+ *
+ * Conventions for every entry point
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    "host" pointers are read during the call only.  The caller owns every
+ *    buffer passed in; the library owns only its workspace (sized at
+ *    wedlm_create) and its cached CUDA graphs.
+ *  - `stream` is a cudaStream_t (passed as void*); work is enqueued on it and
+ *    the call returns without synchronising.  Inputs and outputs of one call
+ *    must not alias, except `seq_len`, which is updated in place.
+ *  - Calls that share one context must not run concurrently (the workspace
+ *    is shared).
+ *  - Return value: WEDLM_OK or an error code; wedlm_last_error() gives a
+ *    message.  Errors found on the device (bad page id, capacity, token out
+ *    of range, non-finite scores) set bits of a device error word that
+ *    wedlm_get_status() reads; the kernels skip the offending access.
+ *  - Matrices are row-major.  Linear weights are [out_features][in_features].
+ *  - Element type of weights, activations and KV pools is the context's
+ *    dtype: WEDLM_BF16 (bfloat16, fp32 accumulation) or WEDLM_FP32.
+ *
+ * Paged KV pool (one per layer): `num_pages` pages, each
+ * [2 (K, V)][n_kv_heads][page_block tokens][head_dim] values.  Inside one
+ * (page, K|V, kv-head) block of page_block*head_dim values, element
+ * (token t, dim d) is at ((t/8)*(head_dim/8) + d/8)*64 + (t%8)*8 + d%8:
+ * 8x8 tiles ordered token-group-major.  This is the layout the tensor-core
+ * attention consumes directly.  page_table[b][j] is the page holding
+ * positions 16j..16j+15 of sequence b.  K is stored after RoPE.
+ */
+#ifndef WEDLM_H
+#define WEDLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  WEDLM_OK = 0,
+  WEDLM_ERR_INVALID_ARG = 1, /* null/misaligned pointer, size out of range  */
+  WEDLM_ERR_CAPACITY = 2,    /* page table cannot hold seq_len + W          */
+  WEDLM_ERR_CUDA = 3,        /* a CUDA call or launch failed                */
+  WEDLM_ERR_NUMERIC = 4,     /* non-finite softmax statistics               */
+  WEDLM_ERR_TIMEOUT = 5,     /* a bounded device wait expired               */
+  WEDLM_ERR_DEVICE = 6       /* device error word non-zero (see bits)       */
+};
+
+/* bits of the device error word */
+enum {
+  WEDLM_DEV_BAD_PAGE = 1,     /* page id outside [0, num_pages)             */
+  WEDLM_DEV_CAPACITY = 2,     /* seq_len + W beyond the page table          */
+  WEDLM_DEV_BAD_TOKEN = 4,    /* token id outside [0, vocab)                */
+  WEDLM_DEV_NUMERIC = 8,      /* non-finite lse / entropy                   */
+  WEDLM_DEV_TIMEOUT = 16,     /* bounded mbarrier / flag wait expired       */
+  WEDLM_DEV_BAD_SEQLEN = 32   /* negative seq_len                           */
+};
+
+enum { WEDLM_BF16 = 0, WEDLM_FP32 = 1 };
+
+typedef struct wedlm_ctx wedlm_ctx;
+
+/* Model and capacity, fixed at create time. */
+typedef struct wedlm_config {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  int32_t window;            /* W, slots per sequence (1..64)               */
+  int32_t page_block;        /* tokens per page; must be 16                 */
+  int32_t max_batch;         /* B_max; B_max * W <= 512                     */
+  int32_t max_pages_per_seq; /* columns of page_table                       */
+  int32_t dtype;             /* WEDLM_BF16 | WEDLM_FP32                     */
+  int32_t qk_norm;           /* 1: per-head RMSNorm on q and k before RoPE  */
+  int32_t mask_id;           /* token id of [M]                             */
+  float rope_theta, rms_eps;
+} wedlm_config;
+
+/* Device pointers to the weights (dtype of the context).  Per-layer fields
+ * are HOST arrays of n_layers device pointers; they are copied at create.
+ * q_norm / k_norm may be NULL when qk_norm = 0.  The weights must stay alive
+ * and unchanged for the context's lifetime. */
+typedef struct wedlm_weights {
+  const void *embed;      /* [vocab][hidden]                                */
+  const void *final_norm; /* [hidden]                                       */
+  const void *lm_head;    /* [vocab][hidden] (untied)                       */
+  const void *const *attn_norm; /* [hidden]                                 */
+  const void *const *w_q;       /* [n_q_heads*head_dim][hidden]             */
+  const void *const *w_k;       /* [n_kv_heads*head_dim][hidden]            */
+  const void *const *w_v;       /* [n_kv_heads*head_dim][hidden]            */
+  const void *const *q_norm;    /* [head_dim]                               */
+  const void *const *k_norm;    /* [head_dim]                               */
+  const void *const *w_o;       /* [hidden][n_q_heads*head_dim]             */
+  const void *const *ffn_norm;  /* [hidden]                                 */
+  const void *const *w_gate;    /* [ffn][hidden]                            */
+  const void *const *w_up;      /* [ffn][hidden]                            */
+  const void *const *w_down;    /* [hidden][ffn]                            */
+} wedlm_weights;
+
+/* Per-row softmax statistics of one window row (LM-head output). */
+typedef struct wedlm_slot_rec {
+  int32_t argmax;  /* token id with the largest logit (lowest id on ties)  */
+  float entropy;   /* H = -sum p ln p, nats                                 */
+  float p_max;     /* probability of argmax                                 */
+  float lse;       /* log-sum-exp of the logits                             */
+} wedlm_slot_rec;
+
+/* Inputs of one step (all device pointers unless noted). */
+typedef struct wedlm_step_in {
+  int32_t batch;               /* B, 1..max_batch                          */
+  int32_t num_pages;           /* pages in each layer's pool               */
+  const int32_t *tokens;       /* [B][W] token ids; masked slots hold [M]  */
+  const int32_t *pos;          /* [B][W] logical positions                 */
+  const uint8_t *observed;     /* [B][W] 1 = observed, 0 = masked          */
+  int32_t *seq_len;            /* [B] committed length; += n_committed     */
+  const int32_t *page_table;   /* [B][max_pages_per_seq]                   */
+  void *const *kv_pools;       /* HOST array of n_layers device pools      */
+  const int32_t *plant_token;  /* [B][W] token to bias per slot (-1: none), or NULL */
+  float plant_bias;            /* added to that token's logit              */
+  float alpha, tau;            /* Eq. 11 distance weight and threshold     */
+} wedlm_step_in;
+
+/* Outputs of one step (device pointers; optional ones may be NULL). */
+typedef struct wedlm_step_out {
+  int32_t *new_tokens;         /* [B][W] window after fill/commit/refill   */
+  int32_t *new_pos;            /* [B][W]                                   */
+  uint8_t *new_observed;       /* [B][W]                                   */
+  int32_t *committed;          /* [B][W] committed ids, -1 after the run   */
+  int32_t *n_committed;        /* [B]                                      */
+  int32_t *perm;               /* [B][W] slot at each physical index, or NULL */
+  uint8_t *filled;             /* [B][W] 1 where a slot was filled, or NULL */
+  wedlm_slot_rec *rows;        /* [B*W] per PHYSICAL row, or NULL          */
+  float *logits;               /* [B*W][vocab] fp32 per physical row, or NULL
+                                  (debug: materialises the logits)         */
+  void *hidden;                /* [B*W][hidden] final residual stream, or NULL */
+} wedlm_step_out;
+
+/* Create a context: validates the config, copies the weight pointers,
+ * allocates the workspace (window K/V scratch, activations, split-K and
+ * split-KV partials, error word) and builds TMA descriptors.
+ * Returns WEDLM_ERR_INVALID_ARG for unsupported shapes. */
+int wedlm_create(const wedlm_config *cfg, const wedlm_weights *w,
+                 wedlm_ctx **out);
+
+void wedlm_destroy(wedlm_ctx *ctx);
+
+/* Message for the last error on this context (never NULL). */
+const char *wedlm_last_error(wedlm_ctx *ctx);
+
+/* Synchronises the stream of the last call, returns the device error word
+ * in *device_error (may be NULL) and clears it.  Returns WEDLM_ERR_DEVICE
+ * when the word was non-zero. */
+int wedlm_get_status(wedlm_ctx *ctx, int32_t *device_error);
+
+/* 1 = launch each step through a cached CUDA graph (default), 0 = eager.
+ * Graphs are keyed by every pointer and scalar of the call. */
+int wedlm_set_graphs(wedlm_ctx *ctx, int enable);
+
+/* Per-kernel timing with CUDA events (forces eager launches while on).
+ * wedlm_get_timings synchronises and writes, for each of `n` kernel kinds
+ * (see WEDLM_KIND_*), the summed milliseconds and launch counts since the
+ * last reset, then resets them. */
+enum {
+  WEDLM_KIND_REORDER = 0, WEDLM_KIND_RMSNORM, WEDLM_KIND_GEMM_QKV,
+  WEDLM_KIND_ATTN, WEDLM_KIND_ATTN_MERGE, WEDLM_KIND_GEMM_O,
+  WEDLM_KIND_GEMM_GATEUP, WEDLM_KIND_GEMM_DOWN, WEDLM_KIND_LMHEAD,
+  WEDLM_KIND_LMHEAD_MERGE, WEDLM_KIND_SELECT, WEDLM_KIND_COMMIT,
+  WEDLM_KIND_COUNT
+};
+int wedlm_set_timing(wedlm_ctx *ctx, int enable);
+int wedlm_get_timings(wedlm_ctx *ctx, float *ms, int32_t *launches, int n);
+
+/* Number of kernel launches one wedlm_step enqueues for batch B. */
+int wedlm_launches_per_step(wedlm_ctx *ctx, int32_t batch);
+
+/* ---- the whole step (rows a1..a7) ------------------------------------- */
+int wedlm_step(wedlm_ctx *ctx, const wedlm_step_in *in, wedlm_step_out *out,
+               void *stream);
+
+/* ---- one row of the step each (tests and composition) ------------------ */
+
+/* Topological Reordering + embedding gather (Key claims §4.1).
+ * perm/inv: [B][W] int32 (device, may be NULL); x_out: [B*W][hidden] in the
+ * physical order; pos_phys: [B*W] logical position of each physical row
+ * (may be NULL). */
+int wedlm_reorder_embed(wedlm_ctx *ctx, int32_t batch, const int32_t *tokens,
+                        const int32_t *pos, const uint8_t *observed,
+                        int32_t *perm, int32_t *inv, void *x_out,
+                        int32_t *pos_phys, void *stream);
+
+/* One decoder layer over the window rows (pre-attention projections with
+ * RoPE at logical positions, paged causal window attention, O projection,
+ * SwiGLU FFN, residuals).  x: [B*W][hidden] (physical order), updated in
+ * place; pos_phys: [B*W]; seq_len: [B] (read only); kv_pool: this layer's
+ * pool.  kv_win_out: [B][2][n_kv][Wp][head_dim] in the page tile layout
+ * (Wp = W rounded up to 16) receives this layer's window K/V, or NULL.
+ * q_out: [B*W][n_q*head_dim], attn_out: [B*W][n_q*head_dim], or NULL. */
+int wedlm_layer(wedlm_ctx *ctx, int32_t layer, int32_t batch, void *x,
+                const int32_t *pos_phys, const int32_t *seq_len,
+                const int32_t *page_table, int32_t num_pages,
+                const void *kv_pool, void *kv_win_out, void *q_out,
+                void *attn_out, void *stream);
+
+/* Paged causal GQA window attention alone (Key claims §3.2, §5.2).
+ * q: [B*W][n_q][head_dim] (RoPE applied); kv_win: [B][2][n_kv][Wp][hd]
+ * tile layout; o: [B*W][n_q*head_dim].  Query row p of sequence b sees
+ * prefix positions 0..seq_len[b]-1 and window rows 0..p. */
+int wedlm_attention(wedlm_ctx *ctx, int32_t batch, const void *q,
+                    const void *kv_pool, const int32_t *page_table,
+                    const int32_t *seq_len, int32_t num_pages,
+                    const void *kv_win, void *o, void *stream);
+
+/* Final RMSNorm + LM head + streaming softmax statistics per row.
+ * x: [B*W][hidden]; plant_token: [B*W] per physical row or NULL;
+ * rows: [B*W] out; logits: [B*W][vocab] fp32 or NULL. */
+int wedlm_lm_head(wedlm_ctx *ctx, int32_t batch, const void *x,
+                  const int32_t *plant_token, float plant_bias,
+                  wedlm_slot_rec *rows, float *logits, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WEDLM_H */

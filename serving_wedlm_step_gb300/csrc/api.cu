@@ -1,0 +1,708 @@
+// libwedlm C ABI: context, workspace, step orchestration, CUDA graphs and
+// per-kernel timing.  See include/wedlm.h for the contract of each call.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "gemm_tc.h"
+#include "internal.h"
+
+using namespace wedlm;
+
+namespace {
+
+struct GraphEntry {
+  std::vector<uint64_t> key;
+  cudaGraphExec_t exec = nullptr;
+  uint64_t last_use = 0;
+};
+
+constexpr int kMaxGraphs = 4;
+constexpr int kMaxEvents = 8192;
+
+}  // namespace
+
+struct wedlm_ctx {
+  wedlm_config cfg{};
+  int es = 2;                 // element size
+  int Wp = 16;                // window rounded up to a page
+  int M_max = 0;
+  int num_sms = 0;
+  int device = 0;
+  const void* embed = nullptr;
+  const void* final_norm = nullptr;
+  const void* lm_head = nullptr;
+  std::vector<LayerWeights> layers;
+  // workspace
+  std::vector<void*> allocs;
+  int* err = nullptr;
+  int32_t *perm = nullptr, *inv = nullptr, *pos_phys = nullptr,
+          *seq_snap = nullptr, *plant_phys = nullptr, *ncommit = nullptr;
+  double* inv_freq = nullptr;
+  float *cosb = nullptr, *sinb = nullptr;
+  void *x = nullptr, *xn = nullptr, *q = nullptr, *o = nullptr, *act = nullptr;
+  void* kv_win = nullptr;
+  size_t win_layer_stride = 0;  // elements
+  float *attn_o = nullptr, *attn_ml = nullptr;
+  int attn_chunk = 0, attn_max_chunks = 0;
+  float* gemm_part = nullptr;
+  size_t gemm_part_elems = 0;
+  int* gemm_counters = nullptr;
+  int vtiles = 0;
+  SoftmaxPart* lm_part = nullptr;
+  wedlm_slot_rec* rows = nullptr;
+  // tensor-core GEMM plans (bf16 contexts)
+  std::unique_ptr<TcPlanSet> tc;
+  // runtime state
+  cudaStream_t last_stream = nullptr;
+  cudaStream_t cap_stream = nullptr;
+  std::string last_error = "ok";
+  bool use_graphs = true;
+  std::vector<GraphEntry> graphs;
+  uint64_t graph_clock = 0;
+  // timing
+  bool timing = false;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> ev_kind;
+  int ev_used = 0;
+  double kind_ms[WEDLM_KIND_COUNT] = {};
+  int kind_launches[WEDLM_KIND_COUNT] = {};
+};
+
+namespace {
+
+int fail(wedlm_ctx* c, int code, const std::string& msg) {
+  if (c) c->last_error = msg;
+  return code;
+}
+
+#define CUDA_TRY(c, expr)                                                     \
+  do {                                                                        \
+    cudaError_t _e = (expr);                                                  \
+    if (_e != cudaSuccess)                                                    \
+      return fail((c), WEDLM_ERR_CUDA,                                        \
+                  std::string(#expr) + ": " + cudaGetErrorString(_e));        \
+  } while (0)
+
+template <typename P>
+cudaError_t walloc(wedlm_ctx* c, P** p, size_t bytes) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, std::max<size_t>(bytes, 256));
+  if (e != cudaSuccess) return e;
+  c->allocs.push_back(v);
+  *p = static_cast<P*>(v);
+  return cudaMemset(v, 0, std::max<size_t>(bytes, 256));
+}
+
+// timing helpers: an event pair around each launch of a kernel kind
+struct Timed {
+  wedlm_ctx* c;
+  int kind;
+  cudaStream_t st;
+  int slot = -1;
+  Timed(wedlm_ctx* c_, int k, cudaStream_t s) : c(c_), kind(k), st(s) {
+    if (c->timing && c->ev_used + 2 <= kMaxEvents) {
+      slot = c->ev_used;
+      c->ev_used += 2;
+      c->ev_kind[slot] = kind;
+      cudaEventRecord(c->ev[slot], st);
+    }
+  }
+  ~Timed() {
+    if (slot >= 0) cudaEventRecord(c->ev[slot + 1], st);
+  }
+};
+
+int choose_splits(const wedlm_ctx* c, int tiles, int M, int N, int K, int kblk) {
+  const int target = 2 * c->num_sms;
+  int s = std::max(1, target / std::max(1, tiles));
+  s = std::min(s, std::max(1, K / (kblk * 4)));
+  while (s > 1 && (size_t)s * M * N > c->gemm_part_elems) --s;
+  return s;
+}
+
+template <typename T>
+int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st) {
+  const int tiles = P.swiglu ? P.N / 128 : (P.N + 127) / 128;
+  P.partial = c->gemm_part;
+  P.counters = c->gemm_counters;
+  P.err = c->err;
+  cudaError_t e;
+  {
+    Timed t(c, kind, st);
+    if (c->cfg.dtype == WEDLM_BF16) {
+      e = launch_gemm_tc(*c->tc, P, kind, st);
+    } else {
+      P.splits = choose_splits(c, tiles, P.M, P.N, P.K, 16);
+      e = launch_gemm_simt<T>(P, st);
+    }
+  }
+  if (e != cudaSuccess)
+    return fail(c, WEDLM_ERR_CUDA, std::string("gemm launch: ") + cudaGetErrorString(e));
+  return WEDLM_OK;
+}
+
+#define LAUNCH(c, kind, st, expr)                                             \
+  do {                                                                        \
+    cudaError_t _e;                                                           \
+    {                                                                         \
+      Timed _t((c), (kind), (st));                                            \
+      _e = (expr);                                                            \
+    }                                                                         \
+    if (_e != cudaSuccess)                                                    \
+      return fail((c), WEDLM_ERR_CUDA,                                        \
+                  std::string(#kind) + ": " + cudaGetErrorString(_e));        \
+  } while (0)
+
+AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
+                   const int32_t* page_table, const int32_t* seq_len,
+                   int num_pages, const void* kv_win, void* o) {
+  const wedlm_config& g = c->cfg;
+  AttnArgs A{};
+  A.B = B; A.W = g.window; A.Wp = c->Wp; A.nq = g.n_q_heads; A.nkv = g.n_kv_heads;
+  A.hd = g.head_dim; A.chunk = c->attn_chunk; A.max_chunks = c->attn_max_chunks;
+  A.num_pages = num_pages; A.max_pages = g.max_pages_per_seq;
+  A.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.head_dim));
+  A.q = q; A.pool = pool; A.page_table = page_table; A.seq_len = seq_len;
+  A.kv_win = kv_win; A.part_o = c->attn_o; A.part_ml = c->attn_ml; A.o = o;
+  A.err = c->err;
+  return A;
+}
+
+// rows a2..a4 for one layer, on workspace activations
+template <typename T>
+int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
+               const int32_t* page_table, int num_pages, const void* pool,
+               void* kv_win_layer, cudaStream_t st) {
+  const wedlm_config& g = c->cfg;
+  const LayerWeights& w = c->layers[l];
+  const int M = B * g.window, H = g.hidden, hd = g.head_dim;
+  const int nq = g.n_q_heads, nkv = g.n_kv_heads;
+  int rc;
+  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+         launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
+  {
+    GemmProblem P{};
+    P.M = M; P.N = (nq + 2 * nkv) * hd; P.K = H; P.X = c->xn;
+    P.A0 = w.w_q; P.A1 = w.w_k; P.A2 = w.w_v;
+    P.seg1 = nq * hd; P.seg2 = (nq + nkv) * hd; P.swiglu = 0;
+    GemmEpi& e = P.epi;
+    e.mode = EPI_QKV; e.q_out = c->q; e.kv_win = kv_win_layer;
+    e.cosb = c->cosb; e.sinb = c->sinb; e.q_norm = w.q_norm; e.k_norm = w.k_norm;
+    e.qk_norm = g.qk_norm; e.W = g.window; e.Wp = c->Wp; e.nq = nq; e.nkv = nkv;
+    e.hd = hd; e.eps = g.rms_eps;
+    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_QKV, st))) return rc;
+  }
+  AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
+                         kv_win_layer, c->o);
+  LAUNCH(c, WEDLM_KIND_ATTN, st, launch_attention<T>(A, st));
+  LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
+  {
+    GemmProblem P{};
+    P.M = M; P.N = H; P.K = nq * hd; P.X = c->o;
+    P.A0 = w.w_o; P.A1 = w.w_o; P.A2 = w.w_o; P.seg1 = H; P.seg2 = H;
+    P.epi.mode = EPI_RESID; P.epi.x = x;
+    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_O, st))) return rc;
+  }
+  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+         launch_rmsnorm<T>(M, H, x, (const T*)w.ffn_norm, g.rms_eps, (T*)c->xn, st));
+  {
+    GemmProblem P{};
+    P.M = M; P.N = 2 * g.ffn; P.K = H; P.X = c->xn;
+    P.A0 = w.w_gate; P.A1 = w.w_up; P.A2 = w.w_up; P.seg1 = P.N; P.seg2 = P.N;
+    P.swiglu = 1;
+    P.epi.mode = EPI_SWIGLU; P.epi.act = c->act;
+    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_GATEUP, st))) return rc;
+  }
+  {
+    GemmProblem P{};
+    P.M = M; P.N = H; P.K = g.ffn; P.X = c->act;
+    P.A0 = w.w_down; P.A1 = w.w_down; P.A2 = w.w_down; P.seg1 = H; P.seg2 = H;
+    P.epi.mode = EPI_RESID; P.epi.x = x;
+    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_DOWN, st))) return rc;
+  }
+  return WEDLM_OK;
+}
+
+template <typename T>
+int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant_phys,
+                float plant_bias, float* logits, cudaStream_t st) {
+  const wedlm_config& g = c->cfg;
+  const int M = B * g.window;
+  int rc;
+  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+         launch_rmsnorm<T>(M, g.hidden, x, (const T*)c->final_norm, g.rms_eps,
+                           (T*)c->xn, st));
+  GemmProblem P{};
+  P.M = M; P.N = g.vocab; P.K = g.hidden; P.X = c->xn;
+  P.A0 = c->lm_head; P.A1 = c->lm_head; P.A2 = c->lm_head;
+  P.seg1 = g.vocab; P.seg2 = g.vocab;
+  GemmEpi& e = P.epi;
+  e.mode = EPI_LMHEAD; e.part = c->lm_part; e.mask_id = g.mask_id;
+  e.vocab = g.vocab; e.plant = plant_phys; e.plant_bias = plant_bias;
+  e.logits = logits;
+  if ((rc = run_gemm<T>(c, P, WEDLM_KIND_LMHEAD, st))) return rc;
+  LAUNCH(c, WEDLM_KIND_LMHEAD_MERGE, st,
+         launch_lmhead_merge(M, c->vtiles, c->lm_part, c->rows, c->err, st));
+  return WEDLM_OK;
+}
+
+int check_step_args(wedlm_ctx* c, const wedlm_step_in* in, const wedlm_step_out* out) {
+  const wedlm_config& g = c->cfg;
+  if (!in || !out) return fail(c, WEDLM_ERR_INVALID_ARG, "null in/out");
+  if (in->batch < 1 || in->batch > g.max_batch)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "batch outside 1..max_batch");
+  if (in->num_pages < 1) return fail(c, WEDLM_ERR_INVALID_ARG, "num_pages < 1");
+  if (!in->tokens || !in->pos || !in->observed || !in->seq_len || !in->page_table ||
+      !in->kv_pools)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "null input pointer");
+  for (int l = 0; l < g.n_layers; ++l)
+    if (!in->kv_pools[l] || ((uintptr_t)in->kv_pools[l] & 15))
+      return fail(c, WEDLM_ERR_INVALID_ARG, "null or misaligned kv pool");
+  if (!out->new_tokens || !out->new_pos || !out->new_observed || !out->committed ||
+      !out->n_committed)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "null output pointer");
+  if ((const void*)out->new_tokens == (const void*)in->tokens ||
+      (const void*)out->new_pos == (const void*)in->pos ||
+      (const void*)out->new_observed == (const void*)in->observed)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "outputs alias inputs");
+  return WEDLM_OK;
+}
+
+template <typename T>
+int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
+                  cudaStream_t st) {
+  const wedlm_config& g = c->cfg;
+  const int B = in->batch, W = g.window, M = B * W;
+  int rc;
+  LAUNCH(c, WEDLM_KIND_REORDER, st,
+         launch_reorder_embed<T>(B, W, g.hidden, g.head_dim, g.vocab,
+                                 g.max_pages_per_seq * kPageBlock, in->tokens,
+                                 in->pos, in->observed, in->seq_len,
+                                 in->plant_token, (const T*)c->embed, c->inv_freq,
+                                 c->perm, c->inv, c->pos_phys, c->seq_snap,
+                                 c->plant_phys, (T*)c->x, c->cosb, c->sinb,
+                                 c->err, st));
+  for (int l = 0; l < g.n_layers; ++l) {
+    void* win = (char*)c->kv_win + (size_t)l * c->win_layer_stride * c->es;
+    if ((rc = layer_impl<T>(c, l, B, (T*)c->x, c->seq_snap, in->page_table,
+                            in->num_pages, in->kv_pools[l], win, st)))
+      return rc;
+  }
+  if ((rc = lmhead_impl<T>(c, B, (const T*)c->x,
+                           in->plant_token ? c->plant_phys : nullptr,
+                           in->plant_bias, out->logits, st)))
+    return rc;
+  SelArgs S{};
+  S.B = B; S.W = W; S.mask_id = g.mask_id; S.alpha = in->alpha; S.tau = in->tau;
+  S.tokens = in->tokens; S.pos = in->pos; S.obs = in->observed;
+  S.seq_snap = c->seq_snap; S.seq_len = in->seq_len; S.inv = c->inv; S.rows = c->rows;
+  S.new_tokens = out->new_tokens; S.new_pos = out->new_pos;
+  S.new_obs = out->new_observed; S.committed = out->committed;
+  S.n_committed = out->n_committed; S.ncommit_ws = c->ncommit; S.filled = out->filled;
+  LAUNCH(c, WEDLM_KIND_SELECT, st, launch_select(S, st));
+  CommitArgs C{};
+  C.B = B; C.W = W; C.Wp = c->Wp; C.nkv = g.n_kv_heads; C.hd = g.head_dim;
+  C.n_layers = g.n_layers; C.max_pages = g.max_pages_per_seq; C.num_pages = in->num_pages;
+  C.win_layer_stride = c->win_layer_stride; C.kv_win = c->kv_win; C.inv = c->inv;
+  C.seq_snap = c->seq_snap; C.ncommit = c->ncommit; C.page_table = in->page_table;
+  C.err = c->err;
+  for (int l = 0; l < g.n_layers; ++l) C.pools.p[l] = in->kv_pools[l];
+  LAUNCH(c, WEDLM_KIND_COMMIT, st, launch_commit<T>(C, st));
+  if (out->perm)
+    CUDA_TRY(c, cudaMemcpyAsync(out->perm, c->perm, (size_t)M * 4,
+                                cudaMemcpyDeviceToDevice, st));
+  if (out->rows)
+    CUDA_TRY(c, cudaMemcpyAsync(out->rows, c->rows, (size_t)M * sizeof(wedlm_slot_rec),
+                                cudaMemcpyDeviceToDevice, st));
+  if (out->hidden)
+    CUDA_TRY(c, cudaMemcpyAsync(out->hidden, c->x, (size_t)M * g.hidden * c->es,
+                                cudaMemcpyDeviceToDevice, st));
+  return WEDLM_OK;
+}
+
+int dispatch_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
+                  cudaStream_t st) {
+  return c->cfg.dtype == WEDLM_BF16 ? step_launches<bf16>(c, in, out, st)
+                                    : step_launches<float>(c, in, out, st);
+}
+
+std::vector<uint64_t> graph_key(const wedlm_ctx* c, const wedlm_step_in* in,
+                                const wedlm_step_out* out) {
+  std::vector<uint64_t> k;
+  auto P = [&](const void* p) { k.push_back((uint64_t)(uintptr_t)p); };
+  auto F = [&](float f) { uint32_t u; memcpy(&u, &f, 4); k.push_back(u); };
+  k.push_back((uint64_t)in->batch);
+  k.push_back((uint64_t)in->num_pages);
+  P(in->tokens); P(in->pos); P(in->observed); P(in->seq_len); P(in->page_table);
+  P(in->plant_token); F(in->plant_bias); F(in->alpha); F(in->tau);
+  for (int l = 0; l < c->cfg.n_layers; ++l) P(in->kv_pools[l]);
+  P(out->new_tokens); P(out->new_pos); P(out->new_observed); P(out->committed);
+  P(out->n_committed); P(out->perm); P(out->filled); P(out->rows); P(out->logits);
+  P(out->hidden);
+  return k;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** out) {
+  if (!cfg || !w || !out) return WEDLM_ERR_INVALID_ARG;
+  *out = nullptr;
+  const wedlm_config& g = *cfg;
+  auto bad = [&](bool cond) { return cond; };
+  if (bad(g.n_layers < 1 || g.n_layers > kMaxLayers) ||
+      bad(g.hidden < 128 || g.hidden % 128) ||
+      bad(g.head_dim != 64 && g.head_dim != 128) ||
+      bad(g.n_kv_heads < 1 || g.n_q_heads % g.n_kv_heads) ||
+      bad((g.n_q_heads * g.head_dim) % 128 || (g.n_kv_heads * g.head_dim) % 128) ||
+      bad(g.ffn < 64 || g.ffn % 64) || bad(g.vocab < 2) ||
+      bad(g.mask_id < 0 || g.mask_id >= g.vocab) ||
+      bad(g.window < 1 || g.window > kMaxWindow) || bad(g.page_block != kPageBlock) ||
+      bad(g.max_batch < 1 || g.max_batch * g.window > kMaxRows) ||
+      bad((g.n_q_heads / g.n_kv_heads) * g.window > 128) ||
+      bad(g.max_pages_per_seq < 1) ||
+      bad(g.dtype != WEDLM_BF16 && g.dtype != WEDLM_FP32) ||
+      bad(!(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f)))
+    return WEDLM_ERR_INVALID_ARG;
+  if (g.dtype == WEDLM_BF16 &&
+      ((g.hidden % 64) || ((g.n_q_heads * g.head_dim) % 64) || (g.ffn % 64)))
+    return WEDLM_ERR_INVALID_ARG;
+  if (!w->embed || !w->final_norm || !w->lm_head || !w->attn_norm || !w->w_q ||
+      !w->w_k || !w->w_v || !w->w_o || !w->ffn_norm || !w->w_gate || !w->w_up ||
+      !w->w_down)
+    return WEDLM_ERR_INVALID_ARG;
+  if (g.qk_norm && (!w->q_norm || !w->k_norm)) return WEDLM_ERR_INVALID_ARG;
+
+  std::unique_ptr<wedlm_ctx> c(new wedlm_ctx());
+  c->cfg = g;
+  c->es = g.dtype == WEDLM_BF16 ? 2 : 4;
+  c->Wp = ((g.window + kPageBlock - 1) / kPageBlock) * kPageBlock;
+  c->M_max = g.max_batch * g.window;
+  c->embed = w->embed; c->final_norm = w->final_norm; c->lm_head = w->lm_head;
+  for (int l = 0; l < g.n_layers; ++l) {
+    LayerWeights lw{};
+    lw.attn_norm = w->attn_norm[l]; lw.w_q = w->w_q[l]; lw.w_k = w->w_k[l];
+    lw.w_v = w->w_v[l]; lw.q_norm = g.qk_norm ? w->q_norm[l] : nullptr;
+    lw.k_norm = g.qk_norm ? w->k_norm[l] : nullptr; lw.w_o = w->w_o[l];
+    lw.ffn_norm = w->ffn_norm[l]; lw.w_gate = w->w_gate[l]; lw.w_up = w->w_up[l];
+    lw.w_down = w->w_down[l];
+    const void* ptrs[] = {lw.attn_norm, lw.w_q, lw.w_k, lw.w_v, lw.w_o, lw.ffn_norm,
+                          lw.w_gate, lw.w_up, lw.w_down};
+    for (const void* p : ptrs)
+      if (!p || ((uintptr_t)p & 15)) return WEDLM_ERR_INVALID_ARG;
+    c->layers.push_back(lw);
+  }
+  wedlm_ctx* C = c.get();
+  if (cudaGetDevice(&C->device) != cudaSuccess) return WEDLM_ERR_CUDA;
+  cudaDeviceGetAttribute(&C->num_sms, cudaDevAttrMultiProcessorCount, C->device);
+  if (C->num_sms <= 0) C->num_sms = 148;
+
+  const size_t M = C->M_max, es = C->es, H = g.hidden, hd = g.head_dim;
+  const size_t qd = (size_t)g.n_q_heads * hd;
+  const size_t max_len = (size_t)g.max_pages_per_seq * kPageBlock;
+  C->attn_chunk = (int)std::max<size_t>(
+      256, ((max_len + 15) / 16 + kPageBlock - 1) / kPageBlock * kPageBlock);
+  C->attn_max_chunks = (int)((max_len + C->attn_chunk - 1) / C->attn_chunk) + 1;
+  const size_t R = (size_t)(g.n_q_heads / g.n_kv_heads) * g.window;
+  C->vtiles = (g.vocab + 127) / 128;
+  C->win_layer_stride = (size_t)g.max_batch * 2 * g.n_kv_heads * C->Wp * hd;
+  C->gemm_part_elems = (size_t)16 << 20;  // 64 MB of fp32 split-K partials
+
+  cudaError_t e = cudaSuccess;
+#define WA(ptr, bytes) if (e == cudaSuccess) e = walloc(C, &(ptr), (bytes))
+  WA(C->err, 256);
+  WA(C->perm, M * 4); WA(C->inv, M * 4); WA(C->pos_phys, M * 4);
+  WA(C->plant_phys, M * 4); WA(C->seq_snap, g.max_batch * 4);
+  WA(C->ncommit, g.max_batch * 4);
+  WA(C->inv_freq, hd / 2 * 8);
+  WA(C->cosb, M * hd / 2 * 4); WA(C->sinb, M * hd / 2 * 4);
+  WA(C->x, M * H * es); WA(C->xn, M * H * es);
+  WA(C->q, M * qd * es); WA(C->o, M * qd * es);
+  WA(C->act, M * g.ffn * es);
+  WA(C->kv_win, C->win_layer_stride * g.n_layers * es);
+  WA(C->attn_o, (size_t)g.max_batch * g.n_kv_heads * C->attn_max_chunks * R * hd * 4);
+  WA(C->attn_ml, (size_t)g.max_batch * g.n_kv_heads * C->attn_max_chunks * R * 2 * 4);
+  WA(C->gemm_part, C->gemm_part_elems * 4);
+  WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
+  WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
+  WA(C->rows, M * sizeof(wedlm_slot_rec));
+#undef WA
+  if (e != cudaSuccess) {
+    wedlm_destroy(c.release());
+    return WEDLM_ERR_CUDA;
+  }
+  std::vector<double> inv_freq(hd / 2);
+  for (size_t i = 0; i < hd / 2; ++i)
+    inv_freq[i] = pow((double)g.rope_theta, -2.0 * (double)i / (double)hd);
+  if (cudaMemcpy(C->inv_freq, inv_freq.data(), hd / 2 * 8, cudaMemcpyHostToDevice) !=
+      cudaSuccess) {
+    wedlm_destroy(c.release());
+    return WEDLM_ERR_CUDA;
+  }
+  if (g.dtype == WEDLM_BF16) {
+    std::string msg;
+    C->tc = make_tc_plans(g, C->layers, C->embed, C->lm_head, C->xn, C->o, C->act,
+                          C->num_sms, C->gemm_part_elems, &msg);
+    if (!C->tc) {
+      wedlm_destroy(c.release());
+      return WEDLM_ERR_CUDA;
+    }
+  }
+  if (cudaStreamCreateWithFlags(&C->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    wedlm_destroy(c.release());
+    return WEDLM_ERR_CUDA;
+  }
+  const char* ng = getenv("WEDLM_NO_GRAPH");
+  if (ng && ng[0] == '1') C->use_graphs = false;
+  *out = c.release();
+  return WEDLM_OK;
+}
+
+void wedlm_destroy(wedlm_ctx* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  for (auto& g : c->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  for (auto e : c->ev) cudaEventDestroy(e);
+  for (void* p : c->allocs) cudaFree(p);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  delete c;
+}
+
+const char* wedlm_last_error(wedlm_ctx* c) {
+  return c ? c->last_error.c_str() : "null context";
+}
+
+int wedlm_get_status(wedlm_ctx* c, int32_t* device_error) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  CUDA_TRY(c, cudaStreamSynchronize(c->last_stream));
+  int32_t word = 0;
+  CUDA_TRY(c, cudaMemcpy(&word, c->err, 4, cudaMemcpyDeviceToHost));
+  CUDA_TRY(c, cudaMemset(c->err, 0, 4));
+  if (device_error) *device_error = word;
+  if (word) return fail(c, WEDLM_ERR_DEVICE, "device error word " + std::to_string(word));
+  return WEDLM_OK;
+}
+
+int wedlm_set_graphs(wedlm_ctx* c, int enable) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  c->use_graphs = enable != 0;
+  return WEDLM_OK;
+}
+
+int wedlm_set_timing(wedlm_ctx* c, int enable) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  if (enable && c->ev.empty()) {
+    c->ev.resize(kMaxEvents);
+    c->ev_kind.assign(kMaxEvents, 0);
+    for (auto& e : c->ev) CUDA_TRY(c, cudaEventCreate(&e));
+  }
+  c->timing = enable != 0;
+  return WEDLM_OK;
+}
+
+static int harvest_events(wedlm_ctx* c) {
+  if (c->ev_used == 0) return WEDLM_OK;
+  CUDA_TRY(c, cudaEventSynchronize(c->ev[c->ev_used - 1]));
+  for (int i = 0; i + 1 < c->ev_used; i += 2) {
+    float ms = 0.f;
+    CUDA_TRY(c, cudaEventElapsedTime(&ms, c->ev[i], c->ev[i + 1]));
+    c->kind_ms[c->ev_kind[i]] += ms;
+    c->kind_launches[c->ev_kind[i]] += 1;
+  }
+  c->ev_used = 0;
+  return WEDLM_OK;
+}
+
+int wedlm_get_timings(wedlm_ctx* c, float* ms, int32_t* launches, int n) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  int rc = harvest_events(c);
+  if (rc) return rc;
+  for (int k = 0; k < WEDLM_KIND_COUNT && k < n; ++k) {
+    if (ms) ms[k] = (float)c->kind_ms[k];
+    if (launches) launches[k] = c->kind_launches[k];
+  }
+  for (int k = 0; k < WEDLM_KIND_COUNT; ++k) { c->kind_ms[k] = 0; c->kind_launches[k] = 0; }
+  return WEDLM_OK;
+}
+
+int wedlm_launches_per_step(wedlm_ctx* c, int32_t batch) {
+  if (!c) return -1;
+  (void)batch;
+  // reorder + per layer (2 norms, 4 GEMMs, attention + merge) + final norm,
+  // LM head + merge, select, commit
+  return 1 + c->cfg.n_layers * 8 + 4 + 1;
+}
+
+int wedlm_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  int rc = check_step_args(c, in, out);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  if (c->timing || !c->use_graphs) {
+    if (c->timing && c->ev_used + 4 * wedlm_launches_per_step(c, in->batch) > kMaxEvents)
+      if ((rc = harvest_events(c))) return rc;
+    return dispatch_step(c, in, out, st);
+  }
+  std::vector<uint64_t> key = graph_key(c, in, out);
+  GraphEntry* hit = nullptr;
+  for (auto& g : c->graphs)
+    if (g.key == key) hit = &g;
+  if (!hit) {
+    // capture on the library's own stream, replay on the caller's
+    cudaGraph_t graph = nullptr;
+    CUDA_TRY(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    rc = dispatch_step(c, in, out, c->cap_stream);
+    cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &graph);
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (ce != cudaSuccess)
+      return fail(c, WEDLM_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(ce));
+    cudaGraphExec_t exec = nullptr;
+    ce = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ce != cudaSuccess)
+      return fail(c, WEDLM_ERR_CUDA, std::string("instantiate: ") + cudaGetErrorString(ce));
+    if ((int)c->graphs.size() >= kMaxGraphs) {
+      auto lru = std::min_element(c->graphs.begin(), c->graphs.end(),
+                                  [](const GraphEntry& a, const GraphEntry& b) {
+                                    return a.last_use < b.last_use;
+                                  });
+      cudaGraphExecDestroy(lru->exec);
+      c->graphs.erase(lru);
+    }
+    c->graphs.push_back(GraphEntry{key, exec, 0});
+    hit = &c->graphs.back();
+  }
+  hit->last_use = ++c->graph_clock;
+  CUDA_TRY(c, cudaGraphLaunch(hit->exec, st));
+  return WEDLM_OK;
+}
+
+int wedlm_reorder_embed(wedlm_ctx* c, int32_t batch, const int32_t* tokens,
+                        const int32_t* pos, const uint8_t* observed, int32_t* perm,
+                        int32_t* inv, void* x_out, int32_t* pos_phys, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  if (batch < 1 || batch > g.max_batch || !tokens || !pos || !observed || !x_out)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad reorder arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  const int M = batch * g.window;
+  // the kernel reads seq_len only for the snapshot; feed it a zero array
+  CUDA_TRY(c, cudaMemsetAsync(c->ncommit, 0, (size_t)batch * 4, st));
+  cudaError_t e;
+  if (g.dtype == WEDLM_BF16)
+    e = launch_reorder_embed<bf16>(batch, g.window, g.hidden, g.head_dim, g.vocab,
+                                   g.max_pages_per_seq * kPageBlock, tokens, pos,
+                                   observed, c->ncommit, nullptr, (const bf16*)c->embed,
+                                   c->inv_freq, c->perm, c->inv, c->pos_phys,
+                                   c->seq_snap, nullptr, (bf16*)x_out, c->cosb,
+                                   c->sinb, c->err, st);
+  else
+    e = launch_reorder_embed<float>(batch, g.window, g.hidden, g.head_dim, g.vocab,
+                                    g.max_pages_per_seq * kPageBlock, tokens, pos,
+                                    observed, c->ncommit, nullptr, (const float*)c->embed,
+                                    c->inv_freq, c->perm, c->inv, c->pos_phys,
+                                    c->seq_snap, nullptr, (float*)x_out, c->cosb,
+                                    c->sinb, c->err, st);
+  if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
+  if (perm) CUDA_TRY(c, cudaMemcpyAsync(perm, c->perm, M * 4, cudaMemcpyDeviceToDevice, st));
+  if (inv) CUDA_TRY(c, cudaMemcpyAsync(inv, c->inv, M * 4, cudaMemcpyDeviceToDevice, st));
+  if (pos_phys)
+    CUDA_TRY(c, cudaMemcpyAsync(pos_phys, c->pos_phys, M * 4, cudaMemcpyDeviceToDevice, st));
+  return WEDLM_OK;
+}
+
+int wedlm_layer(wedlm_ctx* c, int32_t layer, int32_t batch, void* x,
+                const int32_t* pos_phys, const int32_t* seq_len,
+                const int32_t* page_table, int32_t num_pages, const void* kv_pool,
+                void* kv_win_out, void* q_out, void* attn_out, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  if (layer < 0 || layer >= g.n_layers || batch < 1 || batch > g.max_batch || !x ||
+      !pos_phys || !seq_len || !page_table || !kv_pool || num_pages < 1)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad layer arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  const int M = batch * g.window;
+  CUDA_TRY(c, launch_rope_table(M, g.head_dim, pos_phys, c->inv_freq, c->cosb, c->sinb, st));
+  CUDA_TRY(c, cudaMemcpyAsync(c->x, x, (size_t)M * g.hidden * c->es,
+                              cudaMemcpyDeviceToDevice, st));
+  void* win = (char*)c->kv_win + (size_t)layer * c->win_layer_stride * c->es;
+  int rc = g.dtype == WEDLM_BF16
+               ? layer_impl<bf16>(c, layer, batch, (bf16*)c->x, seq_len, page_table,
+                                  num_pages, kv_pool, win, st)
+               : layer_impl<float>(c, layer, batch, (float*)c->x, seq_len, page_table,
+                                   num_pages, kv_pool, win, st);
+  if (rc) return rc;
+  CUDA_TRY(c, cudaMemcpyAsync(x, c->x, (size_t)M * g.hidden * c->es,
+                              cudaMemcpyDeviceToDevice, st));
+  const size_t per_b = (size_t)2 * g.n_kv_heads * c->Wp * g.head_dim * c->es;
+  if (kv_win_out)
+    CUDA_TRY(c, cudaMemcpyAsync(kv_win_out, win, per_b * batch, cudaMemcpyDeviceToDevice, st));
+  const size_t qbytes = (size_t)M * g.n_q_heads * g.head_dim * c->es;
+  if (q_out) CUDA_TRY(c, cudaMemcpyAsync(q_out, c->q, qbytes, cudaMemcpyDeviceToDevice, st));
+  if (attn_out)
+    CUDA_TRY(c, cudaMemcpyAsync(attn_out, c->o, qbytes, cudaMemcpyDeviceToDevice, st));
+  return WEDLM_OK;
+}
+
+int wedlm_attention(wedlm_ctx* c, int32_t batch, const void* q, const void* kv_pool,
+                    const int32_t* page_table, const int32_t* seq_len, int32_t num_pages,
+                    const void* kv_win, void* o, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  if (batch < 1 || batch > g.max_batch || !q || !kv_pool || !page_table || !seq_len ||
+      !kv_win || !o || num_pages < 1)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad attention arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  AttnArgs A = attn_args(c, batch, q, kv_pool, page_table, seq_len, num_pages, kv_win, o);
+  cudaError_t e;
+  {
+    Timed t(c, WEDLM_KIND_ATTN, st);
+    e = g.dtype == WEDLM_BF16 ? launch_attention<bf16>(A, st) : launch_attention<float>(A, st);
+  }
+  if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
+  {
+    Timed t(c, WEDLM_KIND_ATTN_MERGE, st);
+    e = g.dtype == WEDLM_BF16 ? launch_attention_merge<bf16>(A, st)
+                              : launch_attention_merge<float>(A, st);
+  }
+  if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
+  return WEDLM_OK;
+}
+
+int wedlm_lm_head(wedlm_ctx* c, int32_t batch, const void* x, const int32_t* plant_token,
+                  float plant_bias, wedlm_slot_rec* rows, float* logits, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  if (batch < 1 || batch > g.max_batch || !x || !rows)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad lm_head arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  const int M = batch * g.window;
+  int rc = g.dtype == WEDLM_BF16
+               ? lmhead_impl<bf16>(c, batch, (const bf16*)x, plant_token, plant_bias, logits, st)
+               : lmhead_impl<float>(c, batch, (const float*)x, plant_token, plant_bias, logits, st);
+  if (rc) return rc;
+  CUDA_TRY(c, cudaMemcpyAsync(rows, c->rows, (size_t)M * sizeof(wedlm_slot_rec),
+                              cudaMemcpyDeviceToDevice, st));
+  return WEDLM_OK;
+}
+
+}  // extern "C"

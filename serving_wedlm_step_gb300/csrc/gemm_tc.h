@@ -1,0 +1,28 @@
+// Tensor-core (tcgen05) weight-streaming GEMM: plans and launcher.
+#pragma once
+
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace wedlm {
+
+// Everything the bf16 GEMMs need that is fixed at create time.
+struct TcPlanSet {
+  int num_sms = 0;
+  size_t part_elems = 0;
+};
+
+std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
+                                         const std::vector<LayerWeights>& layers,
+                                         const void* embed, const void* lm_head,
+                                         void* xn, void* o, void* act,
+                                         int num_sms, size_t part_elems,
+                                         std::string* msg);
+
+cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind,
+                           cudaStream_t st);
+
+}  // namespace wedlm

@@ -1,0 +1,139 @@
+// Internal launch interfaces of libwedlm (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace wedlm {
+
+enum EpiMode { EPI_RESID = 0, EPI_SWIGLU = 1, EPI_QKV = 2, EPI_LMHEAD = 3 };
+
+// Epilogue of the weight-streaming GEMM Y[m][n] = sum_k X[m][k] W[n][k].
+struct GemmEpi {
+  int mode;
+  void* x;              // RESID: residual stream [M][N], updated in place
+  void* act;            // SWIGLU: out [M][N/2] = silu(gate) * up
+  // QKV
+  void* q_out;          // [M][nq*hd]
+  void* kv_win;         // this layer's window K/V [B][2][nkv][Wp*hd] (tiled)
+  const float* cosb;    // [M][hd/2]
+  const float* sinb;
+  const void* q_norm;   // [hd] or null
+  const void* k_norm;
+  int qk_norm, W, Wp, nq, nkv, hd;
+  float eps;
+  // LMHEAD
+  SoftmaxPart* part;    // [tiles][M]
+  int mask_id, vocab;
+  const int32_t* plant; // [M] or null
+  float plant_bias;
+  float* logits;        // [M][vocab] or null
+};
+
+// One weight-streaming GEMM.  Output features come in tiles of 128 rows of
+// the weight; the rows of a tile come from A0/A1/A2 (q/k/v segments) or,
+// for SWIGLU, rows 0..63 from A0 (gate) and 64..127 from A1 (up).
+struct GemmProblem {
+  int M, N, K;
+  const void* X;        // [M][K]
+  const void* A0;
+  const void* A1;
+  const void* A2;
+  int seg1, seg2;       // segment row boundaries (QKV); N otherwise
+  int swiglu;
+  int splits;
+  float* partial;       // [splits][M][N] fp32 (splits > 1)
+  int* counters;        // [tiles], zero between launches
+  int* err;
+  GemmEpi epi;
+};
+
+struct AttnArgs {
+  int B, W, Wp, nq, nkv, hd, chunk, max_chunks, num_pages, max_pages;
+  float scale_log2;     // log2(e) / sqrt(hd)
+  const void* q;        // [B*W][nq][hd]
+  const void* pool;     // this layer's pool
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  const void* kv_win;   // [B][2][nkv][Wp*hd]
+  float* part_o;        // [B][nkv][max_chunks][G*W][hd]
+  float* part_ml;       // [B][nkv][max_chunks][G*W][2]
+  void* o;              // [B*W][nq*hd]
+  int* err;
+};
+
+struct LayerWeights {
+  const void *attn_norm, *w_q, *w_k, *w_v, *q_norm, *k_norm, *w_o, *ffn_norm,
+      *w_gate, *w_up, *w_down;
+};
+
+// host launchers (one per kernel family); each returns cudaGetLastError()
+template <typename T>
+cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
+                                 int page_cap, const int32_t* tokens,
+                                 const int32_t* pos, const uint8_t* obs,
+                                 const int32_t* seq_len, const int32_t* plant,
+                                 const T* embed, const double* inv_freq,
+                                 int32_t* perm_ws, int32_t* inv_ws,
+                                 int32_t* pos_phys, int32_t* seq_snap,
+                                 int32_t* plant_phys, T* x, float* cosb,
+                                 float* sinb, int* err, cudaStream_t st);
+cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
+                              const double* inv_freq, float* cosb, float* sinb,
+                              cudaStream_t st);
+template <typename T>
+cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
+                           T* y, cudaStream_t st);
+template <typename T>
+cudaError_t launch_gemm_simt(const GemmProblem& P, cudaStream_t st);
+template <typename T>
+cudaError_t launch_attention(const AttnArgs& A, cudaStream_t st);
+template <typename T>
+cudaError_t launch_attention_merge(const AttnArgs& A, cudaStream_t st);
+cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
+                                wedlm_slot_rec* rows, int* err,
+                                cudaStream_t st);
+
+struct SelArgs {
+  int B, W, mask_id;
+  float alpha, tau;
+  const int32_t* tokens;
+  const int32_t* pos;
+  const uint8_t* obs;
+  const int32_t* seq_snap;
+  int32_t* seq_len;
+  const int32_t* inv;
+  const wedlm_slot_rec* rows;
+  int32_t* new_tokens;
+  int32_t* new_pos;
+  uint8_t* new_obs;
+  int32_t* committed;
+  int32_t* n_committed;
+  int32_t* ncommit_ws;
+  uint8_t* filled;
+};
+cudaError_t launch_select(const SelArgs& S, cudaStream_t st);
+
+struct PoolPtrs {
+  void* p[kMaxLayers];
+};
+struct CommitArgs {
+  int B, W, Wp, nkv, hd, n_layers, max_pages, num_pages;
+  size_t win_layer_stride;  // elements per layer of the window scratch
+  const void* kv_win;
+  const int32_t* inv;
+  const int32_t* seq_snap;
+  const int32_t* ncommit;
+  const int32_t* page_table;
+  int* err;
+  PoolPtrs pools;
+};
+template <typename T>
+cudaError_t launch_commit(const CommitArgs& C, cudaStream_t st);
+
+}  // namespace wedlm

@@ -1,0 +1,174 @@
+// Topological Reordering + embedding gather + RoPE table, and RMSNorm.
+//
+// Reordering follows the WeDLM summary page (Key claims, "Topological
+// Reordering ... §4.1, Eq. 5-6"; Method): a stable partition of the window
+// slots, observed slots first, masked slots after, each group in slot order;
+// RoPE angles use each token's LOGICAL position.
+#include "internal.h"
+
+namespace wedlm {
+
+// cos/sin of position `p` for pair i: angle p * inv_freq[i] in float64
+__device__ __forceinline__ void rope_row(int p, int half, const double* inv_freq,
+                                         float* cos_row, float* sin_row) {
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    double s, c;
+    sincos((double)p * inv_freq[i], &s, &c);
+    cos_row[i] = (float)c;
+    sin_row[i] = (float)s;
+  }
+}
+
+// grid (W, B): block (p, b) builds physical row p of sequence b.
+template <typename T>
+__global__ void __launch_bounds__(128)
+reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
+                     const int32_t* __restrict__ tokens,
+                     const int32_t* __restrict__ pos,
+                     const uint8_t* __restrict__ obs,
+                     const int32_t* __restrict__ seq_len,
+                     const int32_t* __restrict__ plant,
+                     const T* __restrict__ embed,
+                     const double* __restrict__ inv_freq,
+                     int32_t* perm_ws, int32_t* inv_ws, int32_t* pos_phys,
+                     int32_t* seq_snap, int32_t* plant_phys, T* x,
+                     float* cosb, float* sinb, int* err) {
+  const int p = blockIdx.x, b = blockIdx.y;
+  __shared__ int s_slot;
+  if (threadIdx.x == 0) {
+    // physical index p -> slot: the p-th observed slot, else the
+    // (p - n_obs)-th masked slot
+    const uint8_t* o = obs + (size_t)b * W;
+    int n_obs = 0;
+    for (int j = 0; j < W; ++j) n_obs += (o[j] != 0);
+    int want_obs = p < n_obs;
+    int rank = want_obs ? p : p - n_obs;
+    int slot = 0;
+    for (int j = 0; j < W; ++j) {
+      if ((o[j] != 0) == (want_obs != 0)) {
+        if (rank == 0) { slot = j; break; }
+        --rank;
+      }
+    }
+    s_slot = slot;
+    const int m = b * W + p;
+    perm_ws[m] = slot;
+    inv_ws[b * W + slot] = p;
+    pos_phys[m] = pos[b * W + slot];
+    if (plant_phys) plant_phys[m] = plant ? plant[b * W + slot] : -1;
+    if (p == 0) {
+      int L = seq_len[b];
+      if (L < 0) { set_err(err, WEDLM_DEV_BAD_SEQLEN); L = 0; }
+      if (L + W > page_cap) set_err(err, WEDLM_DEV_CAPACITY);
+      seq_snap[b] = L;
+    }
+  }
+  __syncthreads();
+  const int slot = s_slot;
+  const int m = b * W + p;
+  int tok = tokens[b * W + slot];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) set_err(err, WEDLM_DEV_BAD_TOKEN);
+    tok = 0;
+  }
+  const int half = hd / 2;
+  rope_row(pos[b * W + slot], half, inv_freq, cosb + (size_t)m * half,
+           sinb + (size_t)m * half);
+  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)tok * H);
+  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)m * H);
+  const int nv = H * (int)sizeof(T) / 16;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = src[i];
+}
+
+template <typename T>
+cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
+                                 int page_cap, const int32_t* tokens,
+                                 const int32_t* pos, const uint8_t* obs,
+                                 const int32_t* seq_len, const int32_t* plant,
+                                 const T* embed, const double* inv_freq,
+                                 int32_t* perm_ws, int32_t* inv_ws,
+                                 int32_t* pos_phys, int32_t* seq_snap,
+                                 int32_t* plant_phys, T* x, float* cosb,
+                                 float* sinb, int* err, cudaStream_t st) {
+  reorder_embed_kernel<T><<<dim3(W, B), 128, 0, st>>>(
+      W, H, hd, vocab, page_cap, tokens, pos, obs, seq_len, plant, embed,
+      inv_freq, perm_ws, inv_ws, pos_phys, seq_snap, plant_phys, x, cosb,
+      sinb, err);
+  return cudaGetLastError();
+}
+
+__global__ void rope_table_kernel(int hd, const int32_t* __restrict__ pos_phys,
+                                  const double* __restrict__ inv_freq,
+                                  float* cosb, float* sinb) {
+  const int m = blockIdx.x, half = hd / 2;
+  rope_row(pos_phys[m], half, inv_freq, cosb + (size_t)m * half,
+           sinb + (size_t)m * half);
+}
+
+cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
+                              const double* inv_freq, float* cosb, float* sinb,
+                              cudaStream_t st) {
+  rope_table_kernel<<<M, 64, 0, st>>>(hd, pos_phys, inv_freq, cosb, sinb);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one block per row, fp32 math.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256)
+rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
+               float eps, T* __restrict__ y) {
+  constexpr int N = 16 / sizeof(T);
+  const int m = blockIdx.x;
+  const T* xr = x + (size_t)m * H;
+  T* yr = y + (size_t)m * H;
+  const int nv = H / N;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    Vec16<T> v = ld16(xr + i * N);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      float f = v.get(k);
+      ss = fmaf(f, f, ss);
+    }
+  }
+  __shared__ float red[32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)H + eps);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+    Vec16<T> v = ld16(xr + i * N), gv = ld16(g + i * N), o;
+#pragma unroll
+    for (int k = 0; k < N; ++k) o.set(k, v.get(k) * r * gv.get(k));
+    st16(yr + i * N, o);
+  }
+}
+
+template <typename T>
+cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
+                           T* y, cudaStream_t st) {
+  rmsnorm_kernel<T><<<M, 256, 0, st>>>(H, x, g, eps, y);
+  return cudaGetLastError();
+}
+
+#define INST(T)                                                               \
+  template cudaError_t launch_reorder_embed<T>(                               \
+      int, int, int, int, int, int, const int32_t*, const int32_t*,           \
+      const uint8_t*, const int32_t*, const int32_t*, const T*, const double*, \
+      int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, T*, float*, float*,   \
+      int*, cudaStream_t);                                                    \
+  template cudaError_t launch_rmsnorm<T>(int, int, const T*, const T*, float, \
+                                         T*, cudaStream_t);
+INST(float)
+INST(bf16)
+#undef INST
+
+}  // namespace wedlm

@@ -1,0 +1,158 @@
+"""GPU parity on Qwen3-8B-shaped bf16 layers (32 q / 8 kv heads of 128,
+hidden 4096, FFN 12288, vocab 151936, QK-norm, RoPE theta 1e6, paged KV in
+blocks of 16), against the CPU oracle (float64 with bf16 rounding mirrored at
+the tensors the CUDA path stores in bf16).  Tolerance 2e-2 absolute."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import (Workload, make_pool_torch, make_state_np, make_weights_torch,
+                   qwen3_layers)
+from tests.gpu_common import (Stats, check_pool_writes, compare_seq, dev, pool_bits,
+                              pool_np, run_step, weights_torch_to_np, within)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def one_layer():
+    s = qwen3_layers(1)
+    w = make_weights_torch(s, seed=0, norm_jitter=0.2)
+    return s, w, weights_torch_to_np(w)
+
+
+def _ctx(s, w, W, max_batch, max_pages):
+    from serving_wedlm_step_gb300.binding import WedlmContext
+    return WedlmContext(s, w, window=W, max_batch=max_batch, max_pages_per_seq=max_pages)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_one_layer_step_matches_oracle(one_layer, seed):
+    """One Qwen3-8B-shaped layer, B=1, prefix 2048, W=16 with 4..12 masked,
+    full step including the 151936-token LM head, Eq. 11, commit, refill."""
+    s, w, w_np = one_layer
+    wl = Workload("one_layer", s, batch=1, window=16, prefix=2048, masked=(4, 12), seed=seed)
+    st = make_state_np(wl)
+    # a committed run at the front of the window in some seeds
+    if seed % 2 == 0:
+        st["obs"][0, :3] = 1
+        st["tokens"][0, :3] = [11, 12, 13]
+    pools = [make_pool_torch(s, st["num_pages"], seed, 0)]
+    ref_pools = [pool_np(p) for p in pools]
+    before = [pool_bits(p) for p in pools]
+    ctx = _ctx(s, w, 16, 1, st["max_pages"])
+    gpu = run_step(ctx, st, pools, st["num_pages"], 0.01, 1.0)
+    assert ctx.status() == 0
+    refs = O.oracle_step(s, w_np, st, ref_pools, 0.01, 1.0)
+    stats = Stats()
+    compare_seq(gpu, 0, 16, refs[0], st, 0.01, 1.0, TOL, stats, s.mask_id, bf16_stored=True)
+    r = refs[0]
+    seqs = [(st["page_table"][0], int(st["seq_len"][0]), r.n_commit,
+             r.k_win[0][r.inv[:r.n_commit]], r.v_win[0][r.inv[:r.n_commit]])]
+    check_pool_writes(before[0], pool_bits(pools[0]), pool_np(pools[0]), seqs, s, TOL, stats,
+                      bf16_stored=True)
+    print(stats)
+
+
+def _pack_window(kw, vw, Wp):
+    """[B][W][nkv][hd] K and V -> the window scratch layout
+    [B][2][nkv][Wp*hd] (page tile order)."""
+    B, W, nkv, hd = kw.shape
+    out = np.zeros((B, 2, nkv, Wp * hd), np.float32)
+    t = np.arange(W)[:, None]
+    d = np.arange(hd)[None, :]
+    off = O.page_elem_offset(t, d, hd)
+    for b in range(B):
+        for h in range(nkv):
+            out[b, 0, h][off] = kw[b, :, h]
+            out[b, 1, h][off] = vw[b, :, h]
+    return out
+
+
+def test_ragged_attention_matches_oracle():
+    """Ragged batch of 32: prefixes U[512, 8192], shuffled page tables,
+    W=16, paged causal GQA attention alone."""
+    s = qwen3_layers(1)
+    wl = Workload("ragged", s, batch=32, window=16, prefix=(512, 8192), masked=(4, 12),
+                  shuffled_pages=True, seed=0)
+    st = make_state_np(wl)
+    B, W, nq, nkv, hd = 32, 16, s.n_q_heads, s.n_kv_heads, s.head_dim
+    pool = make_pool_torch(s, st["num_pages"], 0, 0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    q = torch.randn(B * W, nq, hd, generator=g, device="cuda").to(torch.bfloat16)
+    kw = torch.randn(B, W, nkv, hd, generator=g, device="cuda").to(torch.bfloat16)
+    vw = torch.randn(B, W, nkv, hd, generator=g, device="cuda").to(torch.bfloat16)
+    kw_np, vw_np = kw.float().cpu().numpy(), vw.float().cpu().numpy()
+    win = dev(_pack_window(kw_np, vw_np, 16), torch.bfloat16)
+    # weights are irrelevant for attention alone but a context needs some
+    w = make_weights_torch(s, seed=0)
+    ctx = _ctx(s, w, W, B, st["max_pages"])
+    o = torch.empty(B * W, nq * hd, dtype=torch.bfloat16, device="cuda")
+    ctx.attention(q, pool, dev(st["page_table"]), dev(st["seq_len"]), st["num_pages"], win, o)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    o_np = o.float().cpu().numpy().reshape(B, W, nq, hd)
+    q_np = q.float().cpu().numpy().reshape(B, W, nq, hd)
+    pool_f = pool_np(pool)
+    worst = 0.0
+    for b in range(B):
+        kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
+        ref = O.window_attention(q_np[b], kp, vp, kw_np[b], vw_np[b])
+        worst = max(worst, float(np.abs(o_np[b] - ref).max()))
+    print("ragged attention max err", worst)
+    assert worst <= TOL
+
+
+def test_ragged_layer_matches_oracle(one_layer):
+    """The whole decoder layer at the ragged shape (B=32, 512 window rows),
+    sampled sequences compared with the oracle layer on the same input."""
+    s, w, w_np = one_layer
+    wl = Workload("ragged", s, batch=32, window=16, prefix=(512, 8192), masked=(4, 12),
+                  shuffled_pages=True, seed=3)
+    st = make_state_np(wl)
+    B, W = 32, 16
+    pool = make_pool_torch(s, st["num_pages"], 3, 0)
+    ctx = _ctx(s, w, W, B, st["max_pages"])
+    x = torch.empty(B * W, s.hidden, dtype=torch.bfloat16, device="cuda")
+    pos_phys = torch.empty(B * W, dtype=torch.int32, device="cuda")
+    perm = torch.empty(B, W, dtype=torch.int32, device="cuda")
+    ctx.reorder_embed(dev(st["tokens"]), dev(st["pos"]), dev(st["obs"]), perm, None, x, pos_phys)
+    x_in = x.float().cpu().numpy()
+    win = torch.empty(B, 2, s.n_kv_heads, 16 * s.head_dim, dtype=torch.bfloat16, device="cuda")
+    q_out = torch.empty(B * W, s.n_q_heads * s.head_dim, dtype=torch.bfloat16, device="cuda")
+    a_out = torch.empty_like(q_out)
+    ctx.layer(0, x, pos_phys, dev(st["seq_len"]), dev(st["page_table"]), st["num_pages"],
+              pool, kv_win_out=win, q_out=q_out, attn_out=a_out)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    x_out = x.float().cpu().numpy()
+    pos_np = pos_phys.cpu().numpy()
+    perm_np = perm.cpu().numpy()
+    pool_f = pool_np(pool)
+    store = O.storer("bf16")
+    for b in (0, 7, 19, 31):
+        p_ref, _ = O.topological_reorder(st["obs"][b])
+        assert perm_np[b].tolist() == p_ref.tolist()
+        assert pos_np[b * W:(b + 1) * W].tolist() == st["pos"][b][p_ref].tolist()
+        # the embedding gather is a bit-exact copy
+        emb = w["embed"][torch.from_numpy(st["tokens"][b][p_ref]).long().cuda()].float().cpu().numpy()
+        assert np.array_equal(x_in[b * W:(b + 1) * W], emb)
+        cos, sin = O.rope_cos_sin(st["pos"][b][p_ref], s.head_dim, s.rope_theta)
+        kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
+        xr, k, v, o = O.layer_forward(s, w_np["layers"][0], x_in[b * W:(b + 1) * W].astype(np.float64),
+                                      cos, sin, kp, vp, store)
+        wn = win[b].float().cpu().numpy()
+        off = O.page_elem_offset(np.arange(W)[:, None], np.arange(s.head_dim)[None, :], s.head_dim)
+        kg = np.stack([wn[0, h][off] for h in range(s.n_kv_heads)], 1)
+        vg = np.stack([wn[1, h][off] for h in range(s.n_kv_heads)], 1)
+        # every tensor here is stored in bf16 by both sides
+        e = {"x": within(x_out[b * W:(b + 1) * W], xr, TOL, True),
+             "attn": within(a_out.float().cpu().numpy()[b * W:(b + 1) * W], o.reshape(W, -1),
+                            TOL, True),
+             "k": within(kg, k, TOL, True), "v": within(vg, v, TOL, True)}
+        print(b, e)
+        for name, (val, ok) in e.items():
+            assert ok, (b, name, val)
