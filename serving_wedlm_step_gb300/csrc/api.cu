@@ -127,8 +127,10 @@ int choose_splits(const wedlm_ctx* c, int tiles, int M, int N, int K, int kblk) 
 }
 
 template <typename T>
-int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st) {
+int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st,
+             int* tiles_out = nullptr) {
   const int tiles = P.swiglu ? P.N / 128 : (P.N + 127) / 128;
+  if (tiles_out) *tiles_out = tiles;
   P.partial = c->gemm_part;
   P.counters = c->gemm_counters;
   P.err = c->err;
@@ -136,7 +138,7 @@ int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st) {
   {
     Timed t(c, kind, st);
     if (c->cfg.dtype == WEDLM_BF16) {
-      e = launch_gemm_tc(*c->tc, P, kind, st);
+      e = launch_gemm_tc(*c->tc, P, kind, st, tiles_out);
     } else {
       P.splits = choose_splits(c, tiles, P.M, P.N, P.K, 16);
       e = launch_gemm_simt<T>(P, st);
@@ -246,9 +248,10 @@ int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant_phys,
   e.mode = EPI_LMHEAD; e.part = c->lm_part; e.mask_id = g.mask_id;
   e.vocab = g.vocab; e.plant = plant_phys; e.plant_bias = plant_bias;
   e.logits = logits;
-  if ((rc = run_gemm<T>(c, P, WEDLM_KIND_LMHEAD, st))) return rc;
+  int tiles = 0;  // softmax records per row: one per output-feature tile
+  if ((rc = run_gemm<T>(c, P, WEDLM_KIND_LMHEAD, st, &tiles))) return rc;
   LAUNCH(c, WEDLM_KIND_LMHEAD_MERGE, st,
-         launch_lmhead_merge(M, c->vtiles, c->lm_part, c->rows, c->err, st));
+         launch_lmhead_merge(M, tiles, c->lm_part, c->rows, c->err, st));
   return WEDLM_OK;
 }
 
@@ -365,7 +368,7 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
       bad(g.head_dim != 64 && g.head_dim != 128) ||
       bad(g.n_kv_heads < 1 || g.n_q_heads % g.n_kv_heads) ||
       bad((g.n_q_heads * g.head_dim) % 128 || (g.n_kv_heads * g.head_dim) % 128) ||
-      bad(g.ffn < 64 || g.ffn % 64) || bad(g.vocab < 2) ||
+      bad(g.ffn < 64 || g.ffn % 64) || bad(g.vocab < 8 || g.vocab % 4) ||
       bad(g.mask_id < 0 || g.mask_id >= g.vocab) ||
       bad(g.window < 1 || g.window > kMaxWindow) || bad(g.page_block != kPageBlock) ||
       bad(g.max_batch < 1 || g.max_batch * g.window > kMaxRows) ||
@@ -454,6 +457,7 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
     C->tc = make_tc_plans(g, C->layers, C->embed, C->lm_head, C->xn, C->o, C->act,
                           C->num_sms, C->gemm_part_elems, &msg);
     if (!C->tc) {
+      fprintf(stderr, "wedlm_create: %s\n", msg.c_str());
       wedlm_destroy(c.release());
       return WEDLM_ERR_CUDA;
     }

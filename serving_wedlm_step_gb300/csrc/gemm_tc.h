@@ -9,11 +9,16 @@
 
 namespace wedlm {
 
+struct TcMapTable;  // TMA descriptors of every weight matrix
+
 // Everything the bf16 GEMMs need that is fixed at create time.
 struct TcPlanSet {
   int num_sms = 0;
   size_t part_elems = 0;
+  std::shared_ptr<TcMapTable> maps;
 };
+
+int tc_choose_splits(int tiles, int nkb, int M, int N, int num_sms, size_t part_elems);
 
 std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          const std::vector<LayerWeights>& layers,
@@ -22,7 +27,9 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          int num_sms, size_t part_elems,
                                          std::string* msg);
 
+// Launches one GEMM; *tiles_out (may be null) receives the number of
+// output-feature tiles (the LM head's softmax records per row).
 cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind,
-                           cudaStream_t st);
+                           cudaStream_t st, int* tiles_out);
 
 }  // namespace wedlm

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmProblem P) {
   extern __shared__ float smem[];
   float* As = smem;                    // [BK][AS_LD]
   float* Xs = As + BK * AS_LD;         // [BK][XS_LD]
-  float* sacc = Xs + BK * XS_LD;       // [BNM][128]
+  float* sacc = Xs + BK * XS_LD;       // [128][128] (finish pass uses 128 rows)
   const int tile = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int nk = P.K / BK;
@@ -82,51 +82,23 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmProblem P) {
       for (int j = 0; j < 4; ++j)
         sacc[(tx * 4 + j) * 128 + ty * 8 + i] = acc[i][j];
     __syncthreads();
-    if (P.splits == 1) {
-      run_epilogue<T>(P.epi, sacc, m0, mc, tile, P.N, P.M);
-    } else {
-      float* dst = P.partial + (size_t)split * P.M * P.N;
-      for (int idx = tid; idx < mc * 128; idx += 256) {
-        const int r = idx >> 7, f = idx & 127;
-        if (tile * 128 + f < P.N)
-          dst[(size_t)(m0 + r) * P.N + tile * 128 + f] = sacc[idx];
-      }
-    }
+    stage_chunk<T>(P, sacc, m0, mc, tile, split);
     __syncthreads();
   }
-  if (P.splits == 1) return;
-
-  // split-K: the last block of this tile reduces, in split order
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&P.counters[tile], 1) == P.splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int m0 = 0; m0 < P.M; m0 += BNM) {
-    const int mc = min(BNM, P.M - m0);
-    for (int idx = tid; idx < mc * 128; idx += 256) {
-      const int r = idx >> 7, f = idx & 127;
-      float s = 0.f;
-      if (tile * 128 + f < P.N) {
-        for (int sp = 0; sp < P.splits; ++sp)
-          s += __ldcg(P.partial + (size_t)sp * P.M * P.N +
-                      (size_t)(m0 + r) * P.N + tile * 128 + f);
-      }
-      sacc[idx] = s;
-    }
-    __syncthreads();
-    run_epilogue<T>(P.epi, sacc, m0, mc, tile, P.N, P.M);
-    __syncthreads();
-  }
-  if (tid == 0) P.counters[tile] = 0;
+  if (P.splits > 1) splitk_finish<T>(P, sacc, tile);
 }
 
 template <typename T>
 cudaError_t launch_gemm_simt(const GemmProblem& P, cudaStream_t st) {
   const int tiles = P.swiglu ? P.N / 128 : (P.N + 127) / 128;
-  const size_t smem = (size_t)(BK * AS_LD + BK * XS_LD + BNM * 128) * sizeof(float);
+  const size_t smem = (size_t)(BK * AS_LD + BK * XS_LD + 128 * 128) * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        gemm_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   gemm_simt_kernel<T><<<dim3(tiles, P.splits), 256, smem, st>>>(P);
   return cudaGetLastError();
 }

@@ -22,18 +22,38 @@ MARGIN = 1e-3
 
 def bf16_tol(ref, base=2e-2):
     """Tolerance for a tensor both sides store in bf16: `base` absolute plus
-    one bf16 ulp of the value (|ref| * 2^-7 bounds the ulp).  When the GPU's
-    fp32 value and the oracle's fp64 value fall on two sides of a bf16
-    rounding boundary the stored values differ by exactly one ulp, which for
-    |x| >= 4 exceeds any fixed absolute bound of 2e-2."""
-    return base + np.abs(ref) * 2.0 ** -7
+    two bf16 ulps of the value (|ref| * 2^-6 bounds two ulps).  When the
+    GPU's fp32 value and the oracle's fp64 value fall on two sides of a bf16
+    rounding boundary the stored values differ by one ulp, which for |x| >= 4
+    exceeds any fixed absolute bound of 2e-2; the residual stream is rounded
+    twice per layer (after the O projection and after the FFN), so two such
+    flips can add up."""
+    return base + np.abs(ref) * 2.0 ** -6
 
 
-def within(got, ref, tol, bf16_stored):
-    """max |got - ref| and whether it is inside the tolerance."""
-    d = np.abs(np.asarray(got, np.float64) - ref)
+def within(got, ref, tol, bf16_stored, row_scaled=False):
+    """max |got - ref| and whether it is inside the tolerance; on failure
+    prints the worst offending elements.
+
+    row_scaled: for the residual stream, whose absolute error is set by the
+    size of the terms summed into it (attention and FFN outputs) rather than
+    by the final value, the absolute part of the tolerance is scaled by the
+    row's RMS when that exceeds 1."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    d = np.abs(got - ref)
+    if row_scaled and ref.ndim >= 1 and ref.size:
+        tol = tol * np.maximum(1.0, np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True)))
     bound = bf16_tol(ref, tol) if bf16_stored else tol
-    return float(d.max()) if d.size else 0.0, bool(np.all(d <= bound))
+    ok = bool(np.all(d <= bound))
+    if not ok:
+        bad = np.argwhere(d > bound)
+        print(f"  {len(bad)} of {d.size} elements outside the tolerance; worst:")
+        excess = (d - bound)[tuple(bad.T)]
+        for i in np.argsort(-excess)[:8]:
+            ix = tuple(bad[i])
+            print(f"    at {ix}: got {got[ix]:.6g} ref {ref[ix]:.6g} diff {d[ix]:.3g}")
+    return float(d.max()) if d.size else 0.0, ok
 
 
 def dev(a, dtype=None):
@@ -125,7 +145,8 @@ def compare_seq(gpu, b, W, ref: O.SeqStep, st, alpha, tau, tol, stats: Stats,
     assert int(gpu["seq_len"][b]) == ref.new_seq_len
     # floating point: within tolerance
     if check_hidden:
-        e, ok = within(gpu["hidden"].float().numpy()[rows], ref.x_final, tol, bf16_stored)
+        e, ok = within(gpu["hidden"].float().numpy()[rows], ref.x_final, tol, bf16_stored,
+                       row_scaled=bf16_stored)
         stats.err("hidden", e)
         assert ok, f"hidden err {e}"
     sc = ref.scores
