@@ -35,7 +35,12 @@
  * (token t, dim d) is at ((t/8)*(head_dim/8) + d/8)*64 + (t%8)*8 + d%8:
  * 8x8 tiles ordered token-group-major.  This is the layout the tensor-core
  * attention consumes directly.  page_table[b][j] is the page holding
- * positions 16j..16j+15 of sequence b.  K is stored after RoPE.
+ * positions 16j..16j+15 of sequence b.  K is stored after RoPE.  Positions
+ * at or beyond seq_len inside a sequence's last page must hold finite values
+ * (zeros, say): the attention multiplies them by zero probabilities.
+ *
+ * Supported shapes: head_dim 64 or 128 (fp32) / 128 (bf16); window <= 64;
+ * (n_q_heads / n_kv_heads) * window <= 128; max_batch * window <= 512.
  */
 #ifndef WEDLM_H
 #define WEDLM_H
@@ -178,7 +183,8 @@ enum {
 int wedlm_set_timing(wedlm_ctx *ctx, int enable);
 int wedlm_get_timings(wedlm_ctx *ctx, float *ms, int32_t *launches, int n);
 
-/* Number of kernel launches one wedlm_step enqueues for batch B. */
+/* Number of kernels the most recent wedlm_step enqueued (counted while it
+ * was enqueued or captured; -1 before the first step).  `batch` is unused. */
 int wedlm_launches_per_step(wedlm_ctx *ctx, int32_t batch);
 
 /* ---- the whole step (rows a1..a7) ------------------------------------- */

@@ -56,6 +56,7 @@ struct wedlm_ctx {
   int vtiles = 0;
   SoftmaxPart* lm_part = nullptr;
   wedlm_slot_rec* rows = nullptr;
+  void* zero_page = nullptr;  // 4 KiB of zeros: stands in for missing KV pages
   // tensor-core GEMM plans (bf16 contexts)
   std::unique_ptr<TcPlanSet> tc;
   // runtime state
@@ -72,6 +73,9 @@ struct wedlm_ctx {
   int ev_used = 0;
   double kind_ms[WEDLM_KIND_COUNT] = {};
   int kind_launches[WEDLM_KIND_COUNT] = {};
+  // kernels enqueued by the current / last complete step
+  int launch_count = 0;
+  int last_step_launches = -1;
 };
 
 namespace {
@@ -138,10 +142,13 @@ int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st,
   {
     Timed t(c, kind, st);
     if (c->cfg.dtype == WEDLM_BF16) {
-      e = launch_gemm_tc(*c->tc, P, kind, st, tiles_out);
+      int nl = 1;
+      e = launch_gemm_tc(*c->tc, P, kind, st, tiles_out, &nl);
+      c->launch_count += nl;
     } else {
       P.splits = choose_splits(c, tiles, P.M, P.N, P.K, 16);
       e = launch_gemm_simt<T>(P, st);
+      c->launch_count += 1;
     }
   }
   if (e != cudaSuccess)
@@ -155,11 +162,24 @@ int run_gemm(wedlm_ctx* c, GemmProblem P, int kind, cudaStream_t st,
     {                                                                         \
       Timed _t((c), (kind), (st));                                            \
       _e = (expr);                                                            \
+      (c)->launch_count += 1;                                                 \
     }                                                                         \
     if (_e != cudaSuccess)                                                    \
       return fail((c), WEDLM_ERR_CUDA,                                        \
                   std::string(#kind) + ": " + cudaGetErrorString(_e));        \
   } while (0)
+
+// fp32 contexts: CUDA-core attention; bf16: tensor-core attention
+template <typename T>
+cudaError_t run_attention(wedlm_ctx* c, const AttnArgs& A, cudaStream_t st);
+template <>
+cudaError_t run_attention<float>(wedlm_ctx*, const AttnArgs& A, cudaStream_t st) {
+  return launch_attention<float>(A, st);
+}
+template <>
+cudaError_t run_attention<bf16>(wedlm_ctx* c, const AttnArgs& A, cudaStream_t st) {
+  return launch_attention_tc(A, c->zero_page, st);
+}
 
 AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
                    const int32_t* page_table, const int32_t* seq_len,
@@ -202,7 +222,7 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
   }
   AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
                          kv_win_layer, c->o);
-  LAUNCH(c, WEDLM_KIND_ATTN, st, launch_attention<T>(A, st));
+  LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
   LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
   {
     GemmProblem P{};
@@ -331,8 +351,11 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
 
 int dispatch_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
                   cudaStream_t st) {
-  return c->cfg.dtype == WEDLM_BF16 ? step_launches<bf16>(c, in, out, st)
-                                    : step_launches<float>(c, in, out, st);
+  c->launch_count = 0;
+  const int rc = c->cfg.dtype == WEDLM_BF16 ? step_launches<bf16>(c, in, out, st)
+                                            : step_launches<float>(c, in, out, st);
+  if (rc == WEDLM_OK) c->last_step_launches = c->launch_count;
+  return rc;
 }
 
 std::vector<uint64_t> graph_key(const wedlm_ctx* c, const wedlm_step_in* in,
@@ -377,8 +400,10 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
       bad(g.dtype != WEDLM_BF16 && g.dtype != WEDLM_FP32) ||
       bad(!(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f)))
     return WEDLM_ERR_INVALID_ARG;
+  // bf16: tensor-core GEMMs (K multiple of 64) and attention (head_dim 128)
   if (g.dtype == WEDLM_BF16 &&
-      ((g.hidden % 64) || ((g.n_q_heads * g.head_dim) % 64) || (g.ffn % 64)))
+      ((g.hidden % 64) || ((g.n_q_heads * g.head_dim) % 64) || (g.ffn % 64) ||
+       g.head_dim != 128))
     return WEDLM_ERR_INVALID_ARG;
   if (!w->embed || !w->final_norm || !w->lm_head || !w->attn_norm || !w->w_q ||
       !w->w_k || !w->w_v || !w->w_o || !w->ffn_norm || !w->w_gate || !w->w_up ||
@@ -413,8 +438,9 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   const size_t M = C->M_max, es = C->es, H = g.hidden, hd = g.head_dim;
   const size_t qd = (size_t)g.n_q_heads * hd;
   const size_t max_len = (size_t)g.max_pages_per_seq * kPageBlock;
-  C->attn_chunk = (int)std::max<size_t>(
-      256, ((max_len + 15) / 16 + kPageBlock - 1) / kPageBlock * kPageBlock);
+  // key chunk per attention block: about 1/16 of the capacity, a multiple
+  // of 64 keys (the tensor-core kernel's tile), at least 256
+  C->attn_chunk = (int)std::max<size_t>(256, ((max_len + 15) / 16 + 63) / 64 * 64);
   C->attn_max_chunks = (int)((max_len + C->attn_chunk - 1) / C->attn_chunk) + 1;
   const size_t R = (size_t)(g.n_q_heads / g.n_kv_heads) * g.window;
   C->vtiles = (g.vocab + 127) / 128;
@@ -439,6 +465,7 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
   WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
   WA(C->rows, M * sizeof(wedlm_slot_rec));
+  WA(C->zero_page, 4096);
 #undef WA
   if (e != cudaSuccess) {
     wedlm_destroy(c.release());
@@ -543,9 +570,7 @@ int wedlm_get_timings(wedlm_ctx* c, float* ms, int32_t* launches, int n) {
 int wedlm_launches_per_step(wedlm_ctx* c, int32_t batch) {
   if (!c) return -1;
   (void)batch;
-  // reorder + per layer (2 norms, 4 GEMMs, attention + merge) + final norm,
-  // LM head + merge, select, commit
-  return 1 + c->cfg.n_layers * 8 + 4 + 1;
+  return c->last_step_launches;  // counted while the last step was enqueued
 }
 
 int wedlm_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out, void* stream) {
@@ -679,7 +704,8 @@ int wedlm_attention(wedlm_ctx* c, int32_t batch, const void* q, const void* kv_p
   cudaError_t e;
   {
     Timed t(c, WEDLM_KIND_ATTN, st);
-    e = g.dtype == WEDLM_BF16 ? launch_attention<bf16>(A, st) : launch_attention<float>(A, st);
+    e = g.dtype == WEDLM_BF16 ? run_attention<bf16>(c, A, st)
+                              : run_attention<float>(c, A, st);
   }
   if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
   {

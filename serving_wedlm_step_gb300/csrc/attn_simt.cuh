@@ -129,14 +129,10 @@ attn_simt_kernel(AttnArgs A) {
   }
 }
 
-// DPT variants compiled per element type (fp32: small test shapes; bf16:
-// G*W rows of 64 and 128)
+// DPT variants compiled per element type (fp32 contexts only: bf16 runs
+// the tensor-core attention)
 template <typename T> struct AttnVariants;
 template <> struct AttnVariants<float> {
-  static cudaError_t launch(int dpt, dim3 g, int th, size_t sm, cudaStream_t st,
-                            const AttnArgs& A);
-};
-template <> struct AttnVariants<bf16> {
   static cudaError_t launch(int dpt, dim3 g, int th, size_t sm, cudaStream_t st,
                             const AttnArgs& A);
 };

@@ -59,13 +59,25 @@ __device__ __forceinline__ void st_bf16x32(bf16* dst, const float (&v)[32]) {
   }
 }
 
-// Run the epilogue of one row block (all 4 warps; thread = row m).
+// Epilogue items of a tile: independent pieces of one row's work.
+// RESID: 32-column chunks; SWIGLU: 32-feature chunks (gate + up columns);
+// QKV: heads; LMHEAD: the whole tile (one item).
+__host__ __device__ inline int tc_epi_items(const GemmProblem& P, int ntile) {
+  switch (P.epi.mode) {
+    case EPI_RESID: return ntile / 32;
+    case EPI_SWIGLU: return ntile / 64;
+    case EPI_QKV: return ntile / P.epi.hd;
+    default: return 1;
+  }
+}
+
+// Run the epilogue items [i0, i1) of one row of a tile (thread = row m).
 __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, int tile,
-                                 int ntile) {
+                                 int ntile, int i0, int i1) {
   const GemmEpi& e = P.epi;
   if (e.mode == EPI_RESID) {
     bf16* x = static_cast<bf16*>(e.x) + (size_t)m * P.N + tile * ntile;
-    for (int c = 0; c < ntile; c += 32) {
+    for (int c = 32 * i0; c < 32 * i1; c += 32) {
       float v[32];
       acc_chunk(a, c, v);
       if (!a.valid) continue;
@@ -81,7 +93,7 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
     // columns [0, ntile/2): gate; [ntile/2, ntile): up, same features
     const int half = ntile / 2, F = P.N / 2;
     bf16* out = static_cast<bf16*>(e.act) + (size_t)m * F + tile * half;
-    for (int c = 0; c < half; c += 32) {
+    for (int c = 32 * i0; c < 32 * i1; c += 32) {
       float g[32], u[32];
       acc_chunk(a, c, g);
       acc_chunk(a, half + c, u);
@@ -94,7 +106,7 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
     // pairs (d, d + hd/2) and stores; at most 64 values live per thread
     const int hd = e.hd, heads = ntile / hd, hh = hd / 2;
     const int b = m / e.W, p = m % e.W;
-    for (int lh = 0; lh < heads; ++lh) {
+    for (int lh = i0; lh < i1 && lh < heads; ++lh) {
       const int gh = (tile * ntile) / hd + lh;
       const int kind = gh < e.nq ? 0 : (gh < e.nq + e.nkv ? 1 : 2);
       float rs = 1.f;

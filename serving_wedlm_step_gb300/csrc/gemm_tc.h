@@ -28,8 +28,9 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          std::string* msg);
 
 // Launches one GEMM; *tiles_out (may be null) receives the number of
-// output-feature tiles (the LM head's softmax records per row).
+// output-feature tiles (the LM head's softmax records per row) and
+// *launches_out (may be null) the number of kernels enqueued (2 with split-K).
 cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind,
-                           cudaStream_t st, int* tiles_out);
+                           cudaStream_t st, int* tiles_out, int* launches_out);
 
 }  // namespace wedlm

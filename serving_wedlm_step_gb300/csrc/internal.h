@@ -95,6 +95,9 @@ template <typename T>
 cudaError_t launch_attention(const AttnArgs& A, cudaStream_t st);
 template <typename T>
 cudaError_t launch_attention_merge(const AttnArgs& A, cudaStream_t st);
+// tensor-core attention (bf16, head_dim 128, G*W <= 128, W <= 64,
+// chunk a multiple of 64); zero_page: 4 KiB of zeros in device memory
+cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, cudaStream_t st);
 cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 wedlm_slot_rec* rows, int* err,
                                 cudaStream_t st);

@@ -1,21 +1,23 @@
 // bf16 weight-streaming GEMM on the 5th-generation tensor cores (tcgen05).
 //
 // Y[m][n] = sum_k X[m][k] W[n][k] with few activation rows (M = B*W <= 512)
-// and many weight rows.  A block owns a tile of `ntile` (256, or 128 when
-// M > 256) output features and every activation row: the activation rows
-// take the MMA's M side in blocks of 128 (rows beyond M are zero-filled by
-// the TMA), the tile's weight rows its N side.  Per block:
+// and many weight rows.  Work unit = (tile of `ntile` output features,
+// K split).  The activation rows take the MMA's M side in blocks of 128
+// (rows beyond M are zero-filled by the TMA), the tile's weight rows its N
+// side.  Persistent, warp-specialised: one block per SM loops over work
+// units;
 //   warp 0 / lane 0: TMA producer.  Each pipeline stage is one 64-wide K
 //       slice: the activation row blocks and the tile's weight rows (boxes
-//       of 64 rows, L2 evict-first), all with the 128-byte swizzle, in a ring
-//       of shared-memory stages guarded by full/empty mbarriers;
-//   warp 1 / lane 0: MMA issuer: per stage 4 x tcgen05.mma (K = 16) per row
-//       block into TMEM; a tcgen05.commit frees the stage;
-//   warp 2: TMEM allocation / release;
-//   all 4 warps: epilogue, one activation row per thread (TMEM lane), read
-//       straight from TMEM in 32-column chunks (epilogue_tc.cuh).  With
-//       split-K every block stores its fp32 partial and the last block of
-//       the tile sums them in split order and runs the epilogue.
+//       of 64 rows, L2 evict-first), 128-byte swizzle, in a ring of
+//       shared-memory stages guarded by full/empty mbarriers;
+//   warp 1 / lane 0: MMA issuer: 4 x tcgen05.mma (K = 16) per stage and
+//       row block into one of two TMEM accumulators; a tcgen05.commit frees
+//       each stage, another hands the finished accumulator to the epilogue;
+//   warps 2-5: epilogue, one activation row per thread (TMEM lane quadrant
+//       = warp % 4), straight from TMEM (epilogue_tc.cuh), overlapping the
+//       next unit's mainloop.  With split-K they store the fp32 partial;
+//       splitk_epilogue_kernel then sums the partials in split order and
+//       runs the epilogue with one thread per (row, epilogue item).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -28,16 +30,29 @@ namespace wedlm {
 
 namespace {
 constexpr int kMaxStages = 8;
-constexpr int kBK = 64;                    // K elements per stage (128 bytes)
+constexpr int kBK = 64;                           // K elements per stage (128 bytes)
 constexpr uint32_t kXBlockBytes = 128 * kBK * 2;  // one activation row block
 constexpr uint32_t kWBoxBytes = 64 * kBK * 2;     // one 64-row weight box
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;                     // producer, MMA, 4 epilogue warps
 constexpr int kMaxDynSmem = 221 * 1024;
+
+__device__ __forceinline__ void epi_bar() {       // the 4 epilogue warps only
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// bounded wait that gives up at once after any wait of this block timed out
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
+                                              volatile int* abort) {
+  if (*abort) return false;
+  if (mbar_wait(bar, parity, err)) return true;
+  *abort = 1;
+  return false;
+}
 }  // namespace
 
 struct TcLaunch {
-  int stages, ntile, nrb;
-  uint32_t a_bytes, stage_bytes, tmem_cols;
+  int stages, ntile, nrb, nbuf, tiles;
+  uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -47,26 +62,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   extern __shared__ uint8_t dsm_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_done;
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
   __shared__ uint32_t s_tmem;
-  __shared__ int s_last;
+  __shared__ int s_abort, s_issued, s_consumed;
 
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int tile = blockIdx.x, split = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = P.K / kBK;
-  const int kb0 = (int)((long long)nkb * split / P.splits);
-  const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
-  const int niter = kb1 - kb0;
   const int ntile = L.ntile;
+  const int units = L.tiles * P.splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(&bar_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrive per epilogue warp
+    }
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
     mbar_fence_init();
     tma_prefetch_desc(&mW0);
     tma_prefetch_desc(&mX);
@@ -80,105 +99,143 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
-    const int nbox = ntile / 64;
-    const CUtensorMap* wmap[4];
-    int wrow[4];
-    for (int j = 0; j < nbox; ++j) {
-      if (P.swiglu) {  // first half of the boxes: gate rows, second half: up rows
-        const int hb = nbox / 2, half = ntile / 2;
-        wmap[j] = j < hb ? &mW0 : &mW1;
-        wrow[j] = tile * half + 64 * (j < hb ? j : j - hb);
-      } else {
-        const int g = tile * ntile;
-        if (g < P.seg1) { wmap[j] = &mW0; wrow[j] = g + 64 * j; }
-        else if (g < P.seg2) { wmap[j] = &mW1; wrow[j] = g - P.seg1 + 64 * j; }
-        else { wmap[j] = &mW2; wrow[j] = g - P.seg2 + 64 * j; }
-      }
-    }
-    const uint64_t pol = l2_evict_first_policy();
-    for (int i = 0; i < niter; ++i) {
-      const int s = i % L.stages;
-      const uint32_t ph = (uint32_t)(i / L.stages) & 1u;
-      if (!mbar_wait(&bar_empty[s], ph ^ 1u, P.err)) break;
-      uint8_t* st = base + (size_t)s * L.stage_bytes;
-      mbar_arrive_expect_tx(&bar_full[s], L.stage_bytes);
-      const int kx = (kb0 + i) * kBK;
-      for (int r = 0; r < L.nrb; ++r)
-        tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
-      for (int j = 0; j < nbox; ++j)
-        tma_load_2d_hint(st + L.a_bytes + j * kWBoxBytes, wmap[j], &bar_full[s], kx, wrow[j],
-                         pol);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    const uint32_t idesc = idesc_bf16_m128(ntile);
-    for (int i = 0; i < niter; ++i) {
-      const int s = i % L.stages;
-      const uint32_t ph = (uint32_t)(i / L.stages) & 1u;
-      if (!mbar_wait(&bar_full[s], ph, P.err)) break;
-      tc_fence_after();
-      const uint32_t sa = smem_u32(base + (size_t)s * L.stage_bytes);
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(sa + L.a_bytes + kk * 32);
-        for (int r = 0; r < L.nrb; ++r) {
-          const uint64_t ad = sdesc_sw128(sa + r * kXBlockBytes + kk * 32);
-          tc_mma_f16(tmem + (uint32_t)(r * ntile), ad, bd, idesc, (i | kk) != 0);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const uint64_t pol = l2_evict_first_policy();
+      const int nbox = ntile / 64, hb = nbox / 2, half = ntile / 2;
+      int it = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+        const int tile = u / P.splits, split = u % P.splits;
+        const int kb0 = (int)((long long)nkb * split / P.splits);
+        const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
+        const CUtensorMap* seg = &mW0;
+        int row0 = tile * ntile;
+        if (!P.swiglu) {
+          if (row0 >= P.seg2) { seg = &mW2; row0 -= P.seg2; }
+          else if (row0 >= P.seg1) { seg = &mW1; row0 -= P.seg1; }
         }
-      }
-      tc_commit(&bar_empty[s]);
-    }
-    tc_commit(&bar_done);
-  }
-  __syncwarp();
-
-  // ---------------- epilogue: thread = activation row ----------------
-  const bool ok = __syncthreads_and(mbar_wait(&bar_done, 0, P.err)) != 0;
-  tc_fence_after();
-  if (ok) {
-    for (int r = 0; r < L.nrb; ++r) {
-      const int m = r * 128 + 32 * warp + lane;
-      const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(r * ntile);
-      if (P.splits == 1) {
-        AccRow a{1, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
-        tc_epilogue_rows(P, a, m, tile, ntile);
-      } else {
-        float* dst = P.partial + (size_t)split * P.M * P.N + (size_t)m * P.N + tile * ntile;
-        for (int c = 0; c < ntile; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + (uint32_t)c, v);
-          if (m < P.M) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (tile * ntile + c + 4 * i < P.N)
-                __stcg(reinterpret_cast<float4*>(dst + c) + i,
-                       make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % L.stages;
+          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
+          uint8_t* st = base + (size_t)s * L.stage_bytes;
+          mbar_arrive_expect_tx(&bar_full[s], L.stage_bytes);
+          const int kx = kb * kBK;
+          for (int r = 0; r < L.nrb; ++r)
+            tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
+          for (int j = 0; j < nbox; ++j) {
+            const CUtensorMap* mp;
+            int row;
+            if (P.swiglu) {  // first half of the boxes: gate rows, second half: up rows
+              mp = j < hb ? &mW0 : &mW1;
+              row = tile * half + 64 * (j < hb ? j : j - hb);
+            } else {
+              mp = seg;
+              row = row0 + 64 * j;
+            }
+            tma_load_2d_hint(st + L.a_bytes + j * kWBoxBytes, mp, &bar_full[s], kx, row, pol);
           }
         }
       }
+      s_issued = it;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_bf16_m128(ntile);
+      int it = 0, ul = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++ul) {
+        const int split = u % P.splits;
+        const int kb0 = (int)((long long)nkb * split / P.splits);
+        const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
+        const int buf = ul % L.nbuf, use = ul / L.nbuf;
+        if (!wait_or_abort(&acc_empty[buf], ((uint32_t)use & 1u) ^ 1u, P.err, &s_abort)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + (uint32_t)buf * L.buf_cols;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % L.stages;
+          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          if (!wait_or_abort(&bar_full[s], ph, P.err, &s_abort)) { alive = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(base + (size_t)s * L.stage_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(sa + L.a_bytes + kk * 32);
+            for (int r = 0; r < L.nrb; ++r) {
+              const uint64_t ad = sdesc_sw128(sa + r * kXBlockBytes + kk * 32);
+              tc_mma_f16(d0 + (uint32_t)(r * ntile), ad, bd, idesc, (kb != kb0 || kk) ? 1u : 0u);
+            }
+          }
+          tc_commit(&bar_empty[s]);
+        }
+        tc_commit(&acc_full[buf]);
+      }
+      s_consumed = it;
+    }
+  } else {
+    // ---------------- epilogue warps: thread = activation row ----------------
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    int ul = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
+      const int tile = u / P.splits, split = u % P.splits;
+      const int buf = ul % L.nbuf, use = ul / L.nbuf;
+      // on a timeout keep going without waiting (outputs are then invalid and
+      // the error word says so): the epilogue warps must stay in step at
+      // their named barrier
+      wait_or_abort(&acc_full[buf], (uint32_t)use & 1u, P.err, &s_abort);
+      tc_fence_after();
+      for (int r = 0; r < L.nrb; ++r) {
+        const int m = r * 128 + 32 * q + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols +
+                               (uint32_t)(r * ntile);
+        if (P.splits == 1) {
+          AccRow a{1, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
+          tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
+        } else {
+          float* dst = P.partial + (size_t)split * P.M * P.N + (size_t)m * P.N + tile * ntile;
+          for (int c = 0; c < ntile; c += 32) {
+            float v[32];
+            tmem_ld32(taddr + (uint32_t)c, v);
+            if (m < P.M) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (tile * ntile + c + 4 * i < P.N)
+                  __stcg(reinterpret_cast<float4*>(dst + c) + i,
+                         make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);  // accumulator free for the MMA warp
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, L.tmem_cols);
-  if (!ok || P.splits == 1) return;
-
-  // split-K: the last block of this tile reduces in split order
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&P.counters[tile], 1) == P.splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int r = 0; r < L.nrb; ++r) {
-    const int m = r * 128 + 32 * warp + lane;
-    const float* src = P.partial + (size_t)min(m, P.M - 1) * P.N + tile * ntile;
-    AccRow a{0, 0, src, (size_t)P.M * P.N, P.splits, tile * ntile, P.N, m < P.M};
-    tc_epilogue_rows(P, a, m, tile, ntile);
+  tc_fence_after();
+  if (s_abort && threadIdx.x == 0) {
+    // after a timeout: wait (bounded) for this block's copies still in flight
+    for (int it = s_consumed; it < s_issued; ++it)
+      mbar_wait(&bar_full[it % L.stages], (uint32_t)(it / L.stages) & 1u, P.err);
   }
-  if (threadIdx.x == 0) P.counters[tile] = 0;
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, L.tmem_cols);
+}
+
+// Split-K: sum the partials of every split in split order (deterministic)
+// and run the epilogue.  Grid (tiles * items, row blocks of 128); thread =
+// (activation row, epilogue item).
+__global__ void __launch_bounds__(128)
+splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
+  const int tile = blockIdx.x / items, item = blockIdx.x % items;
+  const int m = blockIdx.y * 128 + threadIdx.x;
+  const float* src = P.partial + (size_t)min(m, P.M - 1) * P.N + tile * ntile;
+  AccRow a{0, 0, src, (size_t)P.M * P.N, P.splits, tile * ntile, P.N, m < P.M};
+  tc_epilogue_rows(P, a, m, tile, ntile, item, item + 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -264,32 +321,38 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
   return p;
 }
 
-// split-K factor: minimise waves x (k-blocks per block + a fixed per-block
-// cost), plus a charge for the partial round trip; >= 4 k-blocks per block
+// split-K factor for the persistent kernel: units = tiles * s are dealt
+// round-robin to num_sms blocks.  Cost in k-block times: the busiest
+// block's k-blocks (+1 per unit for the handoff), plus for s > 1 a second
+// launch and the fp32 partial round trip (s * M * N * 8 bytes through L2,
+// about 12 k-block times per 64 MB); >= 4 k-blocks per unit
 int tc_choose_splits(int tiles, int nkb, int M, int N, int num_sms, size_t part_elems) {
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && (nkb / s < 4 || (size_t)s * M * N > part_elems)) break;
-    const int waves = (tiles * s + num_sms - 1) / num_sms;
+    const int rounds = (tiles * s + num_sms - 1) / num_sms;
     const int kper = (nkb + s - 1) / s;
-    const double cost = (double)waves * (kper + 3.0) + (s > 1 ? 2.0 : 0.0);
+    const double partial_mb = (double)s * M * N * 8.0 / 1e6;
+    const double cost = (double)rounds * (kper + 1.0) + (s > 1 ? 3.0 + 12.0 * partial_mb / 64.0 : 0.0);
     if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
   }
   return best;
 }
 
-// output features per tile for a problem with M activation rows
+// output features per tile: 256 when one 128-row block of activations
+// leaves room for two 256-column TMEM accumulators, else 128; every
+// segment boundary (q|k|v) must fall on a tile boundary
 int tc_tile_width(const GemmProblem& P) {
-  if (P.M > 256) return 128;
+  if (P.M > 128) return 128;
   if (P.swiglu) return (P.N / 2) % 128 == 0 ? 256 : 128;
-  if (P.seg1 % 256 || (P.seg2 - P.seg1) % 256) return 128;
+  if (P.seg1 < P.N && (P.seg1 % 256 || (P.seg2 - P.seg1) % 256)) return 128;
   if (P.seg2 < P.N && (P.N - P.seg2) % 256) return 128;
   return 256;
 }
 
 cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cudaStream_t st,
-                           int* tiles_out) {
+                           int* tiles_out, int* launches_out) {
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
   auto find = [&](const void* w) -> const CUtensorMap* {
@@ -303,21 +366,32 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   TcLaunch L;
   L.ntile = tc_tile_width(P);
   L.nrb = (P.M + 127) / 128;
+  L.buf_cols = (uint32_t)(L.nrb * L.ntile);
+  L.nbuf = L.buf_cols * 2 <= 512 ? 2 : 1;
   L.a_bytes = (uint32_t)L.nrb * kXBlockBytes;
   L.stage_bytes = L.a_bytes + (uint32_t)L.ntile * 128u;
   L.stages = (int)std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024) / L.stage_bytes);
   if (L.stages < 2) return cudaErrorInvalidValue;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(L.nrb * L.ntile)) cols <<= 1;
+  while (cols < L.buf_cols * (uint32_t)L.nbuf) cols <<= 1;
   if (cols > 512) return cudaErrorInvalidValue;
   L.tmem_cols = cols;
   CUtensorMap mx;
   if (!encode_2d(&mx, P.X, P.K, P.M, 128)) return cudaErrorInvalidValue;
-  const int tiles = P.swiglu ? (P.N / 2) / (L.ntile / 2) : (P.N + L.ntile - 1) / L.ntile;
-  if (tiles_out) *tiles_out = tiles;
-  P.splits = tc_choose_splits(tiles, P.K / kBK, P.M, P.N, plans.num_sms, plans.part_elems);
+  L.tiles = P.swiglu ? (P.N / 2) / (L.ntile / 2) : (P.N + L.ntile - 1) / L.ntile;
+  if (tiles_out) *tiles_out = L.tiles;
+  P.splits = tc_choose_splits(L.tiles, P.K / kBK, P.M, P.N, plans.num_sms, plans.part_elems);
+  const int units = L.tiles * P.splits;
+  const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + 1024;
-  gemm_tc_kernel<<<dim3(tiles, P.splits), kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
+  gemm_tc_kernel<<<grid, kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
+  if (launches_out) *launches_out = P.splits > 1 ? 2 : 1;
+  if (P.splits > 1) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int items = tc_epi_items(P, L.ntile);
+    splitk_epilogue_kernel<<<dim3(L.tiles * items, L.nrb), 128, 0, st>>>(P, L.ntile, items);
+  }
   return cudaGetLastError();
 }
 

@@ -1,0 +1,148 @@
+"""Full-size parity on the benchmark workload: the 36-layer Qwen3-8B-shaped
+random-init bf16 stack, prefix 4096, W = 16, batch 8, all slots masked, in
+the launch configuration the benchmark times (the step through its CUDA
+graph).  The oracle cannot run the whole stack in seconds, so:
+  * the step's final hidden state equals the chain of single-layer calls
+    (bitwise: same kernels, deterministic reductions);
+  * sampled layers are compared with the oracle layer on the GPU's own input
+    to that layer (teacher forcing), including the window K/V they produce;
+  * the LM-head records of sampled rows are compared with the oracle's
+    softmax statistics over the full 151936-token vocabulary;
+  * selection, commit and refill equal the oracle's rule applied to the
+    GPU's own records, bit-exact, and the page writes land exactly on the
+    committed positions with the K/V of the window.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import WORKLOADS, make_pool_torch, make_state_np, make_weights_torch
+from tests.gpu_common import (MARGIN, dev, pool_bits, pool_np, run_step, top2_gap, within)
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def full():
+    import dataclasses
+    wl = dataclasses.replace(WORKLOADS["full_stack"], extra_pages=2)
+    s = wl.shape
+    st = make_state_np(wl)
+    # a committed run in two sequences: slots 0..2 observed at L..L+2
+    for b in (1, 5):
+        st["obs"][b, :3] = 1
+        st["tokens"][b, :3] = [101 + b, 202 + b, 303 + b]
+    w = make_weights_torch(s, seed=0, norm_jitter=0.2)
+    pools = [make_pool_torch(s, st["num_pages"], 0, l) for l in range(s.n_layers)]
+    return wl, s, st, w, pools
+
+
+def test_full_stack_step(full):
+    from serving_wedlm_step_gb300.binding import WedlmContext, rows_to_numpy
+    wl, s, st, w, pools = full
+    B, W, M = wl.batch, wl.window, wl.batch * wl.window
+    ctx = WedlmContext(s, w, window=W, max_batch=B, max_pages_per_seq=st["max_pages"])
+    layers = [0, 17, 35]
+    before = {l: pool_bits(pools[l]) for l in layers}
+    # --- layer by layer through the single-row entry points -------------
+    d = {k: dev(st[k]) for k in ("tokens", "pos", "obs", "seq_len", "page_table")}
+    x = torch.empty(M, s.hidden, dtype=torch.bfloat16, device="cuda")
+    pos_phys = torch.empty(M, dtype=torch.int32, device="cuda")
+    perm = torch.empty(B, W, dtype=torch.int32, device="cuda")
+    ctx.reorder_embed(d["tokens"], d["pos"], d["obs"], perm, None, x, pos_phys)
+    x_in, win_out = {}, {}
+    capture = set(layers) | {l + 1 for l in layers}
+    for l in range(s.n_layers):
+        if l in capture:
+            x_in[l] = x.float().cpu().numpy().astype(np.float64)
+        if l in layers:
+            win_out[l] = torch.empty(B, 2, s.n_kv_heads, 16 * s.head_dim,
+                                     dtype=torch.bfloat16, device="cuda")
+        ctx.layer(l, x, pos_phys, d["seq_len"], d["page_table"], st["num_pages"], pools[l],
+                  kv_win_out=win_out.get(l))
+    torch.cuda.synchronize()
+    x_chain = x.clone()
+    # --- the step itself (graph path, as the benchmark runs it) ----------
+    gpu = run_step(ctx, st, pools, st["num_pages"], wl.alpha, wl.tau)
+    assert ctx.status() == 0
+    assert torch.equal(gpu["hidden"].cuda(), x_chain), "step hidden != chained layers"
+    perm_np = perm.cpu().numpy()
+    assert gpu["perm"].numpy().tolist() == perm_np.tolist()
+    # --- sampled layers against the oracle (teacher forced) --------------
+    store = O.storer("bf16")
+    pos_np = pos_phys.cpu().numpy()
+    off = O.page_elem_offset(np.arange(W)[:, None], np.arange(s.head_dim)[None, :], s.head_dim)
+    x_out_last = x_chain.float().cpu().numpy()
+    for l in layers:
+        lw = {k: v.float().cpu().numpy() for k, v in w["layers"][l].items()}
+        pool_f = pool_np(pools[l])
+        for b in (0, 5):
+            rows = slice(b * W, (b + 1) * W)
+            cos, sin = O.rope_cos_sin(pos_np[rows], s.head_dim, s.rope_theta)
+            L = int(st["seq_len"][b])
+            # prefix pages are unchanged by the step below position L
+            kp, vp = O.pool_gather(pool_f, st["page_table"][b], L, s)
+            xr, k, v, _ = O.layer_forward(s, lw, x_in[l][rows], cos, sin, kp, vp, store)
+            wn = win_out[l][b].float().cpu().numpy()
+            kg = np.stack([wn[0, h][off] for h in range(s.n_kv_heads)], 1)
+            vg = np.stack([wn[1, h][off] for h in range(s.n_kv_heads)], 1)
+            x_next = x_in[l + 1][rows] if l + 1 < s.n_layers else x_out_last[rows]
+            for name, (e, ok) in (("k", within(kg, k, TOL, True)), ("v", within(vg, v, TOL, True))):
+                assert ok, (l, b, name, e)
+            e, ok = within(x_next, xr, TOL, True, row_scaled=True, tail=1e-4)
+            assert ok, (l, b, "x", e)
+            print(f"layer {l} seq {b}: ok")
+    # --- LM head records on sampled rows ------------------------------------
+    am, H, pm, lse = rows_to_numpy(gpu["rows"])
+    hfin = x_chain.float().cpu().numpy().astype(np.float64)
+    sample = [0, 17, 63, 64 + 9, M - 1]
+    hn = store(O.rmsnorm(hfin[sample], w["final_norm"].float().cpu().numpy(), s.rms_eps))
+    z = O.lm_head_logits(hn, w["lm_head"].float().cpu().numpy(), s.mask_id)
+    sc = O.softmax_scores(z)
+    gaps = top2_gap(z)
+    for i, r in enumerate(sample):
+        assert abs(lse[r] - sc.lse[i]) <= TOL and abs(H[r] - sc.entropy[i]) <= TOL
+        assert abs(pm[r] - sc.p_max[i]) <= TOL
+        if gaps[i] >= MARGIN:
+            assert am[r] == sc.argmax[i]
+    # --- selection / commit / refill: the rule on the GPU's own records ----
+    for b in range(B):
+        p_ref, inv = O.topological_reorder(st["obs"][b])
+        obs_b = st["obs"][b].astype(bool)
+        gH = np.where(obs_b, np.nan, H[b * W + inv])
+        fill, _ = O.select_eq11(gH, st["pos"][b], st["obs"][b], wl.alpha, wl.tau)
+        assert np.nonzero(gpu["filled"].numpy()[b])[0].tolist() == fill
+        c = O.commit_run(st["obs"][b], st["pos"][b], int(st["seq_len"][b]))
+        assert int(gpu["n_committed"].numpy()[b]) == c
+        nt, npos, nobs = O.refill(st["tokens"][b], st["pos"][b], st["obs"][b], fill,
+                                  am[b * W + inv], c, s.mask_id)
+        assert gpu["new_tokens"].numpy()[b].tolist() == nt.tolist()
+        assert gpu["new_pos"].numpy()[b].tolist() == npos.tolist()
+        assert gpu["new_observed"].numpy()[b].tolist() == nobs.tolist()
+        assert int(gpu["seq_len"][b]) == int(st["seq_len"][b]) + c
+    # --- page writes: placement exact, values = the window K/V -------------
+    for l in layers:
+        after = pool_bits(pools[l])
+        changed = before[l] != after
+        expect = np.zeros_like(changed)
+        pv = expect.reshape(-1, 2, s.n_kv_heads, 16 * s.head_dim)
+        vals = pool_np(pools[l])
+        for b in range(B):
+            c = int(gpu["n_committed"].numpy()[b])
+            if not c:
+                continue
+            L = int(st["seq_len"][b])
+            posn = L + np.arange(c)
+            pages = st["page_table"][b][posn // 16]
+            o2 = O.page_elem_offset((posn % 16)[:, None], np.arange(s.head_dim)[None, :], s.head_dim)
+            pv[pages[:, None, None], :, np.arange(s.n_kv_heads)[None, :, None], o2[:, None, :]] = True
+            k, v = O.pool_gather(vals, st["page_table"][b], L + c, s)
+            wn = win_out[l][b].float().cpu().numpy()
+            # committed slots 0..c-1 sit at physical rows 0..c-1
+            kg = np.stack([wn[0, h][off] for h in range(s.n_kv_heads)], 1)[:c]
+            vg = np.stack([wn[1, h][off] for h in range(s.n_kv_heads)], 1)[:c]
+            assert np.array_equal(k[L:], kg) and np.array_equal(v[L:], vg)
+        assert not np.any(changed & ~expect)
+    ctx.close()
