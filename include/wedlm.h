@@ -231,6 +231,33 @@ int wedlm_lm_head(wedlm_ctx *ctx, int32_t batch, const void *x,
                   const int32_t *plant_token, float plant_bias,
                   wedlm_slot_rec *rows, float *logits, void *stream);
 
+/* ---- attention without any device allocation --------------------------- */
+
+/* Paged causal GQA window attention (bf16, head_dim 128) for callers that
+ * cannot allocate device memory: code that runs where cudaMalloc is not
+ * allowed or not wanted, such as inside a host framework that owns every
+ * allocation, a memory-capped service, or a setting where an allocation
+ * could stall or fail mid-run.  The WeDLM pages have no counterpart for this
+ * entry point; it computes the same result as wedlm_attention (same argument
+ * meanings and layouts, no context needed) but keeps its split-KV partials,
+ * zero page and error word in one file-scope device array of 32 MiB, which
+ * every GPU that loads this library holds until the process exits.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and zeroes its zero page; make that first call
+ *    before any stream capture.
+ *  - Sizes whose partials do not fit in the array (batch * n_kv_heads *
+ *    (n_q_heads/n_kv_heads*window) * 130 * 4 bytes per key chunk, at least
+ *    two chunks) return WEDLM_ERR_CAPACITY; bad arguments WEDLM_ERR_INVALID_ARG.
+ *  - Every call shares the array and it keeps the last call's contents:
+ *    calls that overlap on the GPU (other streams, other threads) race.
+ *  - Page ids outside [0, num_pages) read as zeros and are not reported.
+ *  - Calls no cudaMalloc, cudaFree or allocating library routine. */
+int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q_heads,
+                           int32_t n_kv_heads, int32_t max_pages_per_seq,
+                           int32_t num_pages, const void *q, const void *kv_pool,
+                           const int32_t *page_table, const int32_t *seq_len,
+                           const void *kv_win, void *o, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

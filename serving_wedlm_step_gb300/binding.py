@@ -25,7 +25,7 @@ KINDS = ["reorder", "rmsnorm", "gemm_qkv", "attn", "attn_merge", "gemm_o",
 EXPORTED = ["wedlm_create", "wedlm_destroy", "wedlm_last_error", "wedlm_get_status",
             "wedlm_set_graphs", "wedlm_set_timing", "wedlm_get_timings",
             "wedlm_launches_per_step", "wedlm_step", "wedlm_reorder_embed",
-            "wedlm_layer", "wedlm_attention", "wedlm_lm_head"]
+            "wedlm_layer", "wedlm_attention", "wedlm_lm_head", "wedlm_attention_static"]
 
 
 class Config(ctypes.Structure):
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH):
                                     c_void_p, c_int32, c_void_p, c_void_p, c_void_p]
     lib.wedlm_lm_head.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_float,
                                   c_void_p, c_void_p, c_void_p]
+    lib.wedlm_attention_static.argtypes = [c_int32] * 6 + [c_void_p] * 7
     return lib
 
 
@@ -274,6 +275,19 @@ class WedlmContext:
         self._check(self._lib.wedlm_lm_head(
             self._h, batch, _ptr(x), _ptr(plant_token), plant_bias, _ptr(rows_out),
             _ptr(logits), _stream_handle(stream)))
+
+
+def attention_static(window, n_q_heads, n_kv_heads, max_pages_per_seq, num_pages, q, kv_pool,
+                     page_table, seq_len, kv_win, o, stream=None):
+    """wedlm_attention_static: the window attention with no device
+    allocation at all (scratch in the library's static device array).
+    Raises WedlmError on a non-zero return code."""
+    rc = lib().wedlm_attention_static(
+        seq_len.shape[0], window, n_q_heads, n_kv_heads, max_pages_per_seq, num_pages,
+        _ptr(q), _ptr(kv_pool), _ptr(page_table), _ptr(seq_len), _ptr(kv_win), _ptr(o),
+        _stream_handle(stream))
+    if rc != OK:
+        raise WedlmError(rc, "wedlm_attention_static failed")
 
 
 def rows_to_numpy(rows_tensor):

@@ -1,0 +1,97 @@
+// Paged causal window attention for callers that cannot allocate device
+// memory: everything the kernels need beyond the caller's inputs and
+// outputs lives in one file-scope device array (kAttnStaticScratchBytes),
+// which every GPU that loads this library holds until the process exits.
+//
+// The host never dereferences the array's name (in host code it is only a
+// stand-in); the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, and then passed to the
+// kernels.
+#include <mutex>
+
+#include "internal.h"
+
+namespace wedlm {
+
+namespace {
+constexpr size_t kAttnStaticScratchBytes = (size_t)32 << 20;  // 32 MiB
+constexpr size_t kErrOff = 0;         // device error word (256 B)
+constexpr size_t kZeroOff = 256;      // zero page (4 KiB)
+constexpr size_t kPartOff = 256 + 4096;
+constexpr int kMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_attn_scratch[kAttnStaticScratchBytes];
+
+namespace {
+std::mutex g_mu;
+uint8_t* g_addr[kMaxDevices] = {};
+
+// device address of the scratch array on the current device (set up once)
+int scratch_for_current_device(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return WEDLM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return WEDLM_ERR_CUDA;
+    // the zero page must hold zeros; nothing ever writes it afterwards
+    if (cudaMemset(static_cast<uint8_t*>(p) + kZeroOff, 0, 4096) != cudaSuccess)
+      return WEDLM_ERR_CUDA;
+    g_addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_addr[dev];
+  return WEDLM_OK;
+}
+}  // namespace
+
+}  // namespace wedlm
+
+using namespace wedlm;
+
+extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q_heads,
+                                      int32_t n_kv_heads, int32_t max_pages_per_seq,
+                                      int32_t num_pages, const void* q, const void* kv_pool,
+                                      const int32_t* page_table, const int32_t* seq_len,
+                                      const void* kv_win, void* o, void* stream) {
+  const int hd = 128;
+  if (batch < 1 || window < 1 || window > kMaxWindow || n_kv_heads < 1 ||
+      n_q_heads % n_kv_heads || (n_q_heads / n_kv_heads) * window > 128 ||
+      max_pages_per_seq < 1 || num_pages < 1 || !q || !kv_pool || !page_table || !seq_len ||
+      !kv_win || !o)
+    return WEDLM_ERR_INVALID_ARG;
+  const int Wp = ((window + kPageBlock - 1) / kPageBlock) * kPageBlock;
+  const int R = (n_q_heads / n_kv_heads) * window;
+  const size_t max_len = (size_t)max_pages_per_seq * kPageBlock;
+  // split-KV partials per key chunk: [B][nkv][chunk][R][hd] + [..][R][2]
+  const size_t per_chunk = (size_t)batch * n_kv_heads * R * (hd + 2) * sizeof(float);
+  const size_t fit = (kAttnStaticScratchBytes - kPartOff) / per_chunk;
+  if (fit < 2) return WEDLM_ERR_CAPACITY;  // sizes beyond what the scratch holds
+  // chunks of at least 256 keys (multiple of 64); one extra for the window
+  size_t chunk = (max_len + (fit - 1) - 1) / (fit - 1);
+  chunk = ((chunk + 63) / 64) * 64;
+  if (chunk < 256) chunk = 256;
+  const int max_chunks = (int)((max_len + chunk - 1) / chunk) + 1;
+  if ((size_t)max_chunks > fit) return WEDLM_ERR_CAPACITY;
+
+  uint8_t* scratch = nullptr;
+  int rc = scratch_for_current_device(&scratch);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch + kErrOff, 0, 4, st) != cudaSuccess) return WEDLM_ERR_CUDA;
+  float* part_o = reinterpret_cast<float*>(scratch + kPartOff);
+  float* part_ml = part_o + (size_t)batch * n_kv_heads * max_chunks * R * hd;
+
+  AttnArgs A{};
+  A.B = batch; A.W = window; A.Wp = Wp; A.nq = n_q_heads; A.nkv = n_kv_heads; A.hd = hd;
+  A.chunk = (int)chunk; A.max_chunks = max_chunks; A.num_pages = num_pages;
+  A.max_pages = max_pages_per_seq;
+  A.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128)
+  A.q = q; A.pool = kv_pool; A.page_table = page_table; A.seq_len = seq_len;
+  A.kv_win = kv_win; A.part_o = part_o; A.part_ml = part_ml; A.o = o;
+  A.err = reinterpret_cast<int*>(scratch + kErrOff);
+  if (launch_attention_tc(A, scratch + kZeroOff, st) != cudaSuccess) return WEDLM_ERR_CUDA;
+  if (launch_attention_merge<bf16>(A, st) != cudaSuccess) return WEDLM_ERR_CUDA;
+  return WEDLM_OK;
+}
