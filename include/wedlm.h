@@ -240,14 +240,15 @@ int wedlm_lm_head(wedlm_ctx *ctx, int32_t batch, const void *x,
  * could stall or fail mid-run.  The WeDLM pages have no counterpart for this
  * entry point; it computes the same result as wedlm_attention (same argument
  * meanings and layouts, no context needed) but keeps its split-KV partials,
- * zero page and error word in one file-scope device array of 32 MiB, which
+ * zero page and error word in one file-scope device array of 16 MiB, which
  * every GPU that loads this library holds until the process exits.
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and zeroes its zero page; make that first call
  *    before any stream capture.
- *  - Sizes whose partials do not fit in the array (batch * n_kv_heads *
- *    (n_q_heads/n_kv_heads*window) * 130 * 4 bytes per key chunk, at least
- *    two chunks) return WEDLM_ERR_CAPACITY; bad arguments WEDLM_ERR_INVALID_ARG.
+ *  - Sizes whose partials do not fit in the array ((SM count + batch *
+ *    n_kv_heads) segments of (n_q_heads/n_kv_heads*window) rows x 130 floats,
+ *    plus a small table) return WEDLM_ERR_CAPACITY; bad arguments
+ *    WEDLM_ERR_INVALID_ARG.
  *  - Every call shares the array and it keeps the last call's contents:
  *    calls that overlap on the GPU (other streams, other threads) race.
  *  - Page ids outside [0, num_pages) read as zeros and are not reported.

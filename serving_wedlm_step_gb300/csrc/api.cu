@@ -50,6 +50,7 @@ struct wedlm_ctx {
   size_t win_layer_stride = 0;  // elements
   float *attn_o = nullptr, *attn_ml = nullptr;
   int attn_chunk = 0, attn_max_chunks = 0;
+  int* attn_seg_table = nullptr;  // tensor-core attention: [B*nkv][2]
   float* gemm_part = nullptr;
   size_t gemm_part_elems = 0;
   int* gemm_counters = nullptr;
@@ -178,7 +179,7 @@ cudaError_t run_attention<float>(wedlm_ctx*, const AttnArgs& A, cudaStream_t st)
 }
 template <>
 cudaError_t run_attention<bf16>(wedlm_ctx* c, const AttnArgs& A, cudaStream_t st) {
-  return launch_attention_tc(A, c->zero_page, st);
+  return launch_attention_tc(A, c->zero_page, c->num_sms, st);  // attention + merge
 }
 
 AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
@@ -193,6 +194,8 @@ AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
   A.q = q; A.pool = pool; A.page_table = page_table; A.seq_len = seq_len;
   A.kv_win = kv_win; A.part_o = c->attn_o; A.part_ml = c->attn_ml; A.o = o;
   A.err = c->err;
+  A.min_tiles = 2;
+  A.seg_table = c->attn_seg_table;
   return A;
 }
 
@@ -222,8 +225,14 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
   }
   AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
                          kv_win_layer, c->o);
-  LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
-  LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
+  if (g.dtype == WEDLM_BF16) {
+    // tensor-core attention and its segment merge: two kernels
+    LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
+    c->launch_count += 1;
+  } else {
+    LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
+    LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
+  }
   {
     GemmProblem P{};
     P.M = M; P.N = H; P.K = nq * hd; P.X = c->o;
@@ -459,8 +468,14 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   WA(C->q, M * qd * es); WA(C->o, M * qd * es);
   WA(C->act, M * g.ffn * es);
   WA(C->kv_win, C->win_layer_stride * g.n_layers * es);
-  WA(C->attn_o, (size_t)g.max_batch * g.n_kv_heads * C->attn_max_chunks * R * hd * 4);
-  WA(C->attn_ml, (size_t)g.max_batch * g.n_kv_heads * C->attn_max_chunks * R * 2 * 4);
+  // split-KV partials: per (sequence, kv head, chunk) for the CUDA-core
+  // attention; per segment (at most one per SM plus one per unit) for the
+  // tensor-core attention
+  const size_t units = (size_t)g.max_batch * g.n_kv_heads;
+  const size_t slots = std::max(units * C->attn_max_chunks, (size_t)C->num_sms + units);
+  WA(C->attn_o, slots * R * hd * 4);
+  WA(C->attn_ml, slots * R * 2 * 4);
+  WA(C->attn_seg_table, units * 2 * 4);
   WA(C->gemm_part, C->gemm_part_elems * 4);
   WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
   WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
@@ -708,10 +723,9 @@ int wedlm_attention(wedlm_ctx* c, int32_t batch, const void* q, const void* kv_p
                               : run_attention<float>(c, A, st);
   }
   if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
-  {
+  if (g.dtype != WEDLM_BF16) {  // the tensor-core launcher merges itself
     Timed t(c, WEDLM_KIND_ATTN_MERGE, st);
-    e = g.dtype == WEDLM_BF16 ? launch_attention_merge<bf16>(A, st)
-                              : launch_attention_merge<float>(A, st);
+    e = launch_attention_merge<float>(A, st);
   }
   if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
   return WEDLM_OK;

@@ -65,6 +65,9 @@ struct AttnArgs {
   float* part_ml;       // [B][nkv][max_chunks][G*W][2]
   void* o;              // [B*W][nq*hd]
   int* err;
+  // tensor-core (stream-K) attention: partials per segment
+  int min_tiles;        // fewest 64-key tiles a block is given
+  int* seg_table;       // [B*nkv][2]: first segment id, segment count
 };
 
 struct LayerWeights {
@@ -95,9 +98,12 @@ template <typename T>
 cudaError_t launch_attention(const AttnArgs& A, cudaStream_t st);
 template <typename T>
 cudaError_t launch_attention_merge(const AttnArgs& A, cudaStream_t st);
-// tensor-core attention (bf16, head_dim 128, G*W <= 128, W <= 64,
-// chunk a multiple of 64); zero_page: 4 KiB of zeros in device memory
-cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, cudaStream_t st);
+// tensor-core attention (bf16, head_dim 128, G*W <= 128, W <= 64) and its
+// segment merge (two kernels); grid = blocks (one per SM); zero_page: 4 KiB
+// of zeros in device memory.  part_o / part_ml must hold grid + B*nkv
+// segments of G*W rows.
+cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
+                                cudaStream_t st);
 cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 wedlm_slot_rec* rows, int* err,
                                 cudaStream_t st);

@@ -14,7 +14,7 @@
 namespace wedlm {
 
 namespace {
-constexpr size_t kAttnStaticScratchBytes = (size_t)32 << 20;  // 32 MiB
+constexpr size_t kAttnStaticScratchBytes = (size_t)16 << 20;  // 16 MiB
 constexpr size_t kErrOff = 0;         // device error word (256 B)
 constexpr size_t kZeroOff = 256;      // zero page (4 KiB)
 constexpr size_t kPartOff = 256 + 4096;
@@ -63,35 +63,37 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
     return WEDLM_ERR_INVALID_ARG;
   const int Wp = ((window + kPageBlock - 1) / kPageBlock) * kPageBlock;
   const int R = (n_q_heads / n_kv_heads) * window;
-  const size_t max_len = (size_t)max_pages_per_seq * kPageBlock;
-  // split-KV partials per key chunk: [B][nkv][chunk][R][hd] + [..][R][2]
-  const size_t per_chunk = (size_t)batch * n_kv_heads * R * (hd + 2) * sizeof(float);
-  const size_t fit = (kAttnStaticScratchBytes - kPartOff) / per_chunk;
-  if (fit < 2) return WEDLM_ERR_CAPACITY;  // sizes beyond what the scratch holds
-  // chunks of at least 256 keys (multiple of 64); one extra for the window
-  size_t chunk = (max_len + (fit - 1) - 1) / (fit - 1);
-  chunk = ((chunk + 63) / 64) * 64;
-  if (chunk < 256) chunk = 256;
-  const int max_chunks = (int)((max_len + chunk - 1) / chunk) + 1;
-  if ((size_t)max_chunks > fit) return WEDLM_ERR_CAPACITY;
+  if (Wp > 64 || batch * window > kMaxRows) return WEDLM_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    return WEDLM_ERR_CUDA;
+  // segment table + partials of at most (blocks + units) segments of R rows
+  const size_t units = (size_t)batch * n_kv_heads;
+  const size_t table_bytes = ((units * 2 * sizeof(int) + 255) / 256) * 256;
+  const size_t slots = (size_t)sms + units;
+  const size_t need = kPartOff + table_bytes + slots * R * (hd + 2) * sizeof(float);
+  if (need > kAttnStaticScratchBytes) return WEDLM_ERR_CAPACITY;  // beyond the array
 
   uint8_t* scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch + kErrOff, 0, 4, st) != cudaSuccess) return WEDLM_ERR_CUDA;
-  float* part_o = reinterpret_cast<float*>(scratch + kPartOff);
-  float* part_ml = part_o + (size_t)batch * n_kv_heads * max_chunks * R * hd;
+  int* seg_table = reinterpret_cast<int*>(scratch + kPartOff);
+  float* part_o = reinterpret_cast<float*>(scratch + kPartOff + table_bytes);
+  float* part_ml = part_o + slots * R * hd;
 
   AttnArgs A{};
   A.B = batch; A.W = window; A.Wp = Wp; A.nq = n_q_heads; A.nkv = n_kv_heads; A.hd = hd;
-  A.chunk = (int)chunk; A.max_chunks = max_chunks; A.num_pages = num_pages;
-  A.max_pages = max_pages_per_seq;
+  A.num_pages = num_pages; A.max_pages = max_pages_per_seq;
   A.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128)
   A.q = q; A.pool = kv_pool; A.page_table = page_table; A.seq_len = seq_len;
   A.kv_win = kv_win; A.part_o = part_o; A.part_ml = part_ml; A.o = o;
   A.err = reinterpret_cast<int*>(scratch + kErrOff);
-  if (launch_attention_tc(A, scratch + kZeroOff, st) != cudaSuccess) return WEDLM_ERR_CUDA;
-  if (launch_attention_merge<bf16>(A, st) != cudaSuccess) return WEDLM_ERR_CUDA;
+  A.min_tiles = 2;
+  A.seg_table = seg_table;
+  if (launch_attention_tc(A, scratch + kZeroOff, sms, st) != cudaSuccess) return WEDLM_ERR_CUDA;
   return WEDLM_OK;
 }

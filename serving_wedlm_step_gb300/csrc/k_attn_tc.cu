@@ -5,24 +5,27 @@
 // one kv head (G = nq/nkv q heads x W window rows, physical order) attend to
 // every cached prefix position and, causally, to the window (§3.2).
 //
-// Block = (sequence b, kv head, key chunk); chunks 0..ceil(L/chunk)-1 cover
-// the prefix, the last one the window.  Warp roles:
-//   warp 8 / lane 0: producer: each 64-key tile is 4 pages of K and 4 of V
-//       (4 KiB each, already in the 8x8-tile operand layout), copied with
-//       cp.async.bulk into 4-stage K and V rings; missing or invalid pages
-//       come from a zero page;
-//   warp 9 / lane 0: MMA issuer: S = Q K^T (M = 128 query rows, N = 64 keys,
-//       K = head_dim) into one of two TMEM score buffers, then O_tile = P V
-//       (N = head_dim, K = 64 keys; V as an MN-major operand) into one of
-//       two TMEM output buffers;
+// Work = unit (sequence b, kv head) x 64-key tiles: ceil(L_b/64) prefix
+// tiles, then one window tile.  Stream-K: the units' tiles are laid end to
+// end and every block (one per SM) takes an equal contiguous share, so a
+// block processes runs ("segments") of consecutive tiles of one unit; O, the
+// running max and the sum stay in registers across a segment and each
+// segment writes one unnormalised partial, combined by attn_seg_merge_kernel.
+// Warp roles:
 //   warps 0-7: online softmax.  Warps q and q+4 share TMEM lane quadrant q
 //       (query rows 32q..32q+31, thread = row): warp q takes key columns
 //       0-31 of each tile and head dims 0-63 of O, warp q+4 the other halves;
-//       they exchange only the row max of each tile.  Scores come from TMEM,
-//       the running max / sums live in the log2 domain, P goes to shared
-//       memory in bf16 and O accumulates in registers with the rescale.
-// The block writes an unnormalised partial (O, running max, sum) that the
-// split-KV merge combines.
+//       they exchange only the row max of each tile.  They also stage Q at
+//       the start of each segment.  P goes to shared memory in bf16 (double
+//       buffered); O accumulates in registers with the rescale;
+//   warp 8 / lane 0: producer: a prefix tile is 4 pages of K and 4 of V
+//       (4 KiB each, already in the 8x8-tile operand layout), copied with
+//       cp.async.bulk into 4-stage K and V rings; missing or invalid pages
+//       come from a zero page; the window tile comes from the window scratch;
+//   warp 9 / lane 0: MMA issuer: S = Q K^T (M = 128 query rows, N = keys,
+//       K = head_dim) into one of two TMEM score buffers, then O_tile = P V
+//       (N = head_dim; V as an MN-major operand) into one of two TMEM output
+//       buffers.
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -31,56 +34,93 @@ namespace wedlm {
 namespace {
 constexpr int kTile = 64;                  // keys per prefix tile (4 pages)
 constexpr int kStages = 4;
-constexpr int kThreads = 320;            // 8 softmax warps, producer, MMA
+constexpr int kThreads = 320;              // 8 softmax warps, producer, MMA
 constexpr uint32_t kQBytes = 128 * 128 * 2;        // 128 rows x 128 dims
 constexpr uint32_t kPBytes = 128 * kTile * 2;      // 128 rows x 64 keys
 constexpr uint32_t kKVBytes = kTile * 128 * 2;     // one K or V tile
 constexpr uint32_t kOffP = kQBytes;
-constexpr uint32_t kOffK = kOffP + kPBytes;
+constexpr uint32_t kOffK = kOffP + 2 * kPBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-constexpr uint32_t kSmemBytes = kOffV + kStages * kKVBytes;   // 176 KB
+constexpr uint32_t kSmemBytes = kOffV + kStages * kKVBytes;   // 192 KB
 constexpr uint32_t kPageBytes = 16 * 128 * 2;                 // 4 KiB
 constexpr uint32_t kTmemCols = 512;  // S: 2 x 64 columns; O: 2 x 128 columns
+constexpr int kMaxB = kMaxRows;      // sequences (<= rows)
+constexpr int kPagesPerTile = kTile / kPageBlock;
+constexpr int kPrefTiles = 1024;     // tiles whose page ids are staged up front
 }  // namespace
 
-struct AttnTcArgs {
-  AttnArgs A;
-  const void* zero_page;   // 4 KiB of zeros
+// Split of the flattened tile sequence over the blocks; every block and the
+// segment table agree on it.
+struct StreamSplit {
+  long long total;  // tiles of all units
+  int G;            // blocks that get work
+  __device__ long long begin(int c) const { return (long long)c * total / G; }
+  __device__ int owner(long long g) const {  // block holding global tile g
+    int c = (int)((g * G) / total);
+    while (c + 1 < G && begin(c + 1) <= g) ++c;
+    while (c > 0 && begin(c) > g) --c;
+    return c;
+  }
 };
+
+__device__ __forceinline__ int seq_len_clamped(const AttnArgs& A, int b) {
+  return max(0, min(A.seq_len[b], A.max_pages * kPageBlock));
+}
+__device__ __forceinline__ int seq_tiles(const AttnArgs& A, int b) {
+  return (seq_len_clamped(A, b) + kTile - 1) / kTile + 1;
+}
 
 __device__ __forceinline__ uint32_t idesc_pv() {  // M=128, N=128, B MN-major
   return idesc_bf16_m128(128) | (1u << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
-  const AttnArgs& A = args.A;
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const void* zero_page) {
   extern __shared__ uint8_t dsm_raw[];
   __shared__ __align__(8) uint64_t k_full[kStages], k_empty[kStages];
   __shared__ __align__(8) uint64_t v_full[kStages], v_empty[kStages];
   __shared__ __align__(8) uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  __shared__ __align__(8) uint64_t p_full, p_empty;
+  __shared__ __align__(8) uint64_t p_full[2], p_empty[2], q_full, q_empty;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_issued[2], s_done[2];  // K/V tiles copied / consumed
   __shared__ float s_red[2][2][128];      // [tile parity][half][row]: row max
-  __shared__ float s_lsum[2][128];        // [half][row]: final row sums
+  __shared__ float s_lsum[2][128];        // [half][row]: segment row sums
+  __shared__ long long s_tstart[kMaxB];   // first global tile of sequence b
+  __shared__ int s_pages[kPrefTiles * kPagesPerTile];  // page ids (-1: none)
+  __shared__ int s_segbase[kMaxB];        // first segment id of sequence b
+  __shared__ StreamSplit s_split;
 
-  const int b = blockIdx.z, kvh = blockIdx.y, c = blockIdx.x;
   const int hd = 128, G = A.nq / A.nkv, W = A.W, R = G * W;
-  const int L = max(0, min(A.seq_len[b], A.max_pages * kPageBlock));
-  const int n_pre = (L + A.chunk - 1) / A.chunk;
-  if (c > n_pre) return;  // no work for this chunk (uniform for the block)
-  const bool window = (c == n_pre);
-  const int k0 = window ? 0 : c * A.chunk;
-  const int k1 = window ? W : min(L, k0 + A.chunk);
-  const int ntiles = window ? 1 : (k1 - k0 + kTile - 1) / kTile;
-  const int win_keys = A.Wp;  // keys of the window tile (multiple of 16)
-
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    // the plan: tiles per sequence, the block split and the segment ids
+    long long acc = 0;
+    for (int b = 0; b < A.B; ++b) {
+      s_tstart[b] = acc;
+      acc += (long long)seq_tiles(A, b) * A.nkv;
+    }
+    StreamSplit sp;
+    sp.total = acc;
+    const long long by_min = (acc + A.min_tiles - 1) / A.min_tiles;
+    sp.G = (int)min((long long)gridDim.x, max(1LL, by_min));
+    s_split = sp;
+    int sid = 0;
+    for (int b = 0; b < A.B; ++b) {
+      s_segbase[b] = sid;
+      const int T = seq_tiles(A, b);
+      for (int h = 0; h < A.nkv; ++h) {
+        const long long u0 = s_tstart[b] + (long long)h * T;
+        const int n = sp.owner(u0 + T - 1) - sp.owner(u0) + 1;
+        if (blockIdx.x == 0) {
+          A.seg_table[(b * A.nkv + h) * 2 + 0] = sid;
+          A.seg_table[(b * A.nkv + h) * 2 + 1] = n;
+        }
+        sid += n;
+      }
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
@@ -88,33 +128,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 8);
       mbar_init(&o_full[i], 1); mbar_init(&o_free[i], 8);
+      mbar_init(&p_full[i], 8); mbar_init(&p_empty[i], 1);
     }
-    mbar_init(&p_full, 8);
-    mbar_init(&p_empty, 1);
+    mbar_init(&q_full, 8);
+    mbar_init(&q_empty, 1);
     s_abort = 0;
     s_issued[0] = s_issued[1] = s_done[0] = s_done[1] = 0;
     mbar_fence_init();
   }
+  __syncthreads();
+  const StreamSplit sp = s_split;
+  if ((int)blockIdx.x >= sp.G) return;  // uniform for the block
   if (warp == 0) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  // stage Q (rows >= R zero) in the K-major 8x8-core layout: core (r/8, d/8)
-  // at (r/8)*2048 + (d/8)*128 + (r%8)*16 bytes
-  {
-    const bf16* q = static_cast<const bf16*>(A.q);
-    for (int idx = threadIdx.x; idx < 128 * 16; idx += kThreads) {
-      const int r = idx >> 4, d8 = idx & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int g = r / W, p = r % W;
-        v = *reinterpret_cast<const uint4*>(q + ((size_t)(b * W + p) * A.nq + kvh * G + g) * hd +
-                                            d8 * 8);
-      }
-      *reinterpret_cast<uint4*>(base + (r >> 3) * 2048 + d8 * 128 + (r & 7) * 16) = v;
-    }
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -127,6 +155,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
     return false;
   };
 
+  const long long g0 = sp.begin(blockIdx.x);
+  const int ntiles = (int)(sp.begin(blockIdx.x + 1) - g0);
+  // position of a block tile: sequence, kv head, tile within the unit and
+  // tiles of the unit; found once, then advanced tile by tile
+  struct Cur { int b, kvh, t, T, L; };
+  Cur first;
+  {
+    first.b = 0;
+    while (first.b + 1 < A.B && s_tstart[first.b + 1] <= g0) ++first.b;
+    first.L = seq_len_clamped(A, first.b);
+    first.T = (first.L + kTile - 1) / kTile + 1;
+    const long long off = g0 - s_tstart[first.b];
+    first.kvh = (int)(off / first.T);
+    first.t = (int)(off % first.T);
+  }
+  auto advance = [&](Cur& c) {
+    if (++c.t == c.T) {
+      c.t = 0;
+      if (++c.kvh == A.nkv) {
+        c.kvh = 0;
+        if (c.b + 1 < A.B) {
+          c.L = seq_len_clamped(A, ++c.b);
+          c.T = (c.L + kTile - 1) / kTile + 1;
+        }
+      }
+    }
+  };
+
+  // page ids of the block's first kPrefTiles tiles, loaded and checked by
+  // every thread at once so the producer never waits on a global load
+  for (int e = threadIdx.x; e < min(ntiles, kPrefTiles) * kPagesPerTile; e += kThreads) {
+    const long long g = g0 + e / kPagesPerTile;
+    int b = 0, hi = A.B - 1;  // last sequence whose first tile is <= g
+    while (b < hi) {
+      const int mid = (b + hi + 1) >> 1;
+      if (s_tstart[mid] <= g) b = mid; else hi = mid - 1;
+    }
+    const int L = seq_len_clamped(A, b), T = (L + kTile - 1) / kTile + 1;
+    const int t = (int)((g - s_tstart[b]) % T);
+    const int t0 = t * kTile + (e % kPagesPerTile) * kPageBlock;
+    int pid = -1;
+    if (t != T - 1 && t0 < L) {
+      pid = A.page_table[(size_t)b * A.max_pages + t0 / kPageBlock];
+      if (pid < 0 || pid >= A.num_pages) {
+        set_err(A.err, WEDLM_DEV_BAD_PAGE);
+        pid = -1;
+      }
+    }
+    s_pages[e] = pid;
+  }
+  __syncthreads();
+
   if (warp == 8) {
     if (lane == 0) {
       // ---------------- producer ----------------
@@ -134,7 +214,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
       const bf16* pool = static_cast<const bf16*>(A.pool);
       const bf16* win = static_cast<const bf16*>(A.kv_win);
       const size_t blockn = (size_t)kPageBlock * hd;
-      for (int i = 0; i < ntiles; ++i) {
+      constexpr int kPg = kPagesPerTile;
+      // page ids of a tile (-1: no page there): staged in shared memory for
+      // the first kPrefTiles tiles, loaded directly beyond that
+      auto tile_pages = [&](int i, const Cur& c, int (&pid)[kPg]) {
+#pragma unroll
+        for (int pg = 0; pg < kPg; ++pg) {
+          if (i < kPrefTiles) {
+            pid[pg] = s_pages[i * kPg + pg];
+          } else {
+            const int t0 = c.t * kTile + pg * kPageBlock;
+            int v = -1;
+            if (c.t != c.T - 1 && t0 < c.L) {
+              v = A.page_table[(size_t)c.b * A.max_pages + t0 / kPageBlock];
+              if (v < 0 || v >= A.num_pages) {
+                set_err(A.err, WEDLM_DEV_BAD_PAGE);
+                v = -1;
+              }
+            }
+            pid[pg] = v;
+          }
+        }
+      };
+      Cur cur = first;
+      for (int i = 0; i < ntiles; ++i, advance(cur)) {
+        int pid[kPg];
+        tile_pages(i, cur, pid);
+        const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
+        const bool window = (t == T - 1);
         const int st = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
         for (int kv = 0; kv < 2; ++kv) {
@@ -142,23 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
           if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
           uint8_t* dst = base + (kv ? kOffV : kOffK) + st * kKVBytes;
           if (window) {
-            const uint32_t bytes = (uint32_t)win_keys * hd * 2;
+            const uint32_t bytes = (uint32_t)A.Wp * hd * 2;
             mbar_arrive_expect_tx(full, bytes);
             bulk_load(dst, win + (((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp * hd, bytes, full,
                       pol);
           } else {
             mbar_arrive_expect_tx(full, kKVBytes);
-            for (int pg = 0; pg < kTile / kPageBlock; ++pg) {
-              const int t0 = k0 + i * kTile + pg * kPageBlock;
-              const void* src = args.zero_page;
-              if (t0 < k1) {
-                const int pidx = t0 / kPageBlock;
-                const int page = A.page_table[(size_t)b * A.max_pages + pidx];
-                if (page >= 0 && page < A.num_pages)
-                  src = pool + (((size_t)page * 2 + kv) * A.nkv + kvh) * blockn;
-                else
-                  set_err(A.err, WEDLM_DEV_BAD_PAGE);
-              }
+#pragma unroll
+            for (int pg = 0; pg < kPg; ++pg) {
+              const void* src =
+                  pid[pg] >= 0 ? (const void*)(pool + (((size_t)pid[pg] * 2 + kv) * A.nkv + kvh) * blockn)
+                               : zero_page;
               bulk_load(dst + pg * kPageBytes, src, kPageBytes, full, pol);
             }
           }
@@ -170,41 +271,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       const uint32_t sq = smem_u32(base);
-      const uint32_t sp = smem_u32(base + kOffP);
-      const int nS = window ? win_keys : kTile;
-      const uint32_t idS = idesc_bf16_m128(nS);
       const uint32_t idPV = idesc_pv();
+      int seg = -1;  // segment counter (Q buffer phases)
+      Cur cs = first;  // position of the next S to issue
       auto issue_s = [&](int i) -> bool {
+        const int t = cs.t, T = cs.T;
+        advance(cs);
+        if (i == 0 || t == 0) {  // a new segment: wait for its Q
+          ++seg;
+          if (!wait(&q_full, (uint32_t)seg & 1u)) return false;
+        }
         const int st = i % kStages, sb = i & 1;
         if (!wait(&k_full[st], (uint32_t)(i / kStages) & 1u)) return false;
         s_done[0] = i + 1;
         if (!wait(&s_free[sb], ((uint32_t)(i >> 1) & 1u) ^ 1u)) return false;
         tc_fence_after();
         const uint32_t sk = smem_u32(base + kOffK + st * kKVBytes);
+        const uint32_t idS = idesc_bf16_m128(t == T - 1 ? A.Wp : kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma_f16(tmem + (uint32_t)(sb * 64), sdesc_noswz(sq + kk * 256, 128, 2048),
                      sdesc_noswz(sk + kk * 256, 128, 2048), idS, kk ? 1u : 0u);
         tc_commit(&s_full[sb]);
         tc_commit(&k_empty[st]);
+        if (i == ntiles - 1 || t == T - 1) tc_commit(&q_empty);  // segment's last S
         return true;
       };
       bool ok = issue_s(0);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        if (i + 1 < ntiles && !issue_s(i + 1)) break;
-        const int st = i % kStages, ob = i & 1;
+      Cur cur = first;
+      for (int i = 0; i < ntiles && ok; ++i, advance(cur)) {
+        const int t = cur.t, T = cur.T;
+        // within a segment the next S goes ahead of this P V; across a
+        // segment boundary it must wait for the next Q, which the softmax
+        // warps stage only after this tile's P V
+        const bool next_same = (i + 1 < ntiles) && (t != T - 1);
+        if (next_same && !issue_s(i + 1)) break;
+        const int st = i % kStages, ob = i & 1, pb = i & 1;
         if (!wait(&v_full[st], (uint32_t)(i / kStages) & 1u)) break;
         s_done[1] = i + 1;
-        if (!wait(&p_full, (uint32_t)i & 1u)) break;
+        if (!wait(&p_full[pb], (uint32_t)(i >> 1) & 1u)) break;
         if (!wait(&o_free[ob], ((uint32_t)(i >> 1) & 1u) ^ 1u)) break;
         tc_fence_after();
         const uint32_t sv = smem_u32(base + kOffV + st * kKVBytes);
-        for (int kk = 0; kk < nS / 16; ++kk)
-          tc_mma_f16(tmem + 128u + (uint32_t)(ob * 128), sdesc_noswz(sp + kk * 256, 128, 1024),
+        const uint32_t spp = smem_u32(base + kOffP + pb * kPBytes);
+        const int nk = (t == T - 1) ? A.Wp : kTile;
+        for (int kk = 0; kk < nk / 16; ++kk)
+          tc_mma_f16(tmem + 128u + (uint32_t)(ob * 128), sdesc_noswz(spp + kk * 256, 128, 1024),
                      sdesc_noswz(sv + kk * 4096, 2048, 128), idPV, kk ? 1u : 0u);
         tc_commit(&o_full[ob]);
         tc_commit(&v_empty[st]);
-        tc_commit(&p_empty);
+        tc_commit(&p_empty[pb]);
+        if (i + 1 < ntiles && !next_same && !issue_s(i + 1)) break;
       }
     }
   } else {
@@ -215,13 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
     const int p_row = valid ? r % W : 0;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     const float sc = A.scale_log2;
+    const int tid = threadIdx.x;                  // 0..255
     float o[64];
 #pragma unroll
     for (int d = 0; d < 64; ++d) o[d] = 0.f;
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
-    uint8_t* prow = base + kOffP + (r >> 3) * 1024 + (r & 7) * 16;
+    int seg = -1;
     auto pair_bar = [&]() {  // warps q and q+4
       asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
+    };
+    auto softmax_bar = [&]() {  // the 8 softmax warps
+      asm volatile("bar.sync 5, 256;" ::: "memory");
     };
     auto accumulate = [&](int i, float alpha) {
       const int ob = i & 1;
@@ -238,8 +359,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
     };
-    for (int i = 0; i < ntiles; ++i) {
-      const int sb = i & 1;
+    Cur cur = first;
+    for (int i = 0; i < ntiles; ++i, advance(cur)) {
+      const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
+      if (i == 0 || t == 0) {
+        // new segment: stage its Q once the previous segment's S MMAs are done
+        ++seg;
+        wait(&q_empty, ((uint32_t)seg & 1u) ^ 1u);
+        const bf16* qg = static_cast<const bf16*>(A.q);
+        for (int idx = tid; idx < 128 * 16; idx += 256) {
+          const int rr = idx >> 4, d8 = idx & 15;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (rr < R) {
+            const int g = rr / W, p = rr % W;
+            v = *reinterpret_cast<const uint4*>(
+                qg + ((size_t)(b * W + p) * A.nq + kvh * G + g) * hd + d8 * 8);
+          }
+          *reinterpret_cast<uint4*>(base + (rr >> 3) * 2048 + d8 * 128 + (rr & 7) * 16) = v;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        softmax_bar();
+        if (lane == 0) mbar_arrive(&q_full);
+#pragma unroll
+        for (int d = 0; d < 64; ++d) o[d] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
+      }
+      const bool window = (t == T - 1);
+      const int L = cur.L;
+      const int sb = i & 1, pb = i & 1;
       wait(&s_full[sb], (uint32_t)(i >> 1) & 1u);
       tc_fence_after();
       float v[32];
@@ -247,60 +395,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      // mask + scale (log2 domain); row max over both halves of the tile
-      const int kbase = window ? 0 : k0 + i * kTile;
-      float hmax = -INFINITY;
+      // mask (only the partial last prefix tile and the window tile need
+      // one), row max over both halves of the tile, scale applied once
+      const int kbase = t * kTile;
+      if (window || kbase + kTile > L) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int jj = h * 32 + j;
-        const bool ok = window ? (jj < W && jj <= p_row) : (kbase + jj < k1);
-        v[j] = ok ? v[j] * sc : -INFINITY;
-        hmax = fmaxf(hmax, v[j]);
+        for (int j = 0; j < 32; ++j) {
+          const int jj = h * 32 + j;
+          const bool ok = window ? (jj < W && jj <= p_row) : (kbase + jj < L);
+          if (!ok) v[j] = -INFINITY;
+        }
       }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mx[k] = fmaxf(fmaxf(v[4 * k], v[4 * k + 1]), fmaxf(v[4 * k + 2], v[4 * k + 3]));
+      const float hmax =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       s_red[i & 1][h][r] = hmax;
       pair_bar();
       const float m_new = fmaxf(m, fmaxf(hmax, s_red[i & 1][h ^ 1][r]));
-      const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
-      float psum = 0.f;
+      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+      // p = 2^(s*scale - m_new); masked scores are -inf and give 0
+      const float nm = (m_new == -INFINITY) ? 0.f : -m_new;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t packed[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float p0 = (v[j] == -INFINITY) ? 0.f : exp2f(v[j] - m_new);
-        const float p1 = (v[j + 1] == -INFINITY) ? 0.f : exp2f(v[j + 1] - m_new);
-        const bf16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
-        psum += __bfloat162float(b0) + __bfloat162float(b1);
-        packed[j >> 1] = (uint32_t)__bfloat16_as_ushort(b0) |
-                         ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+        const float p0 = ex2_approx(fmaf(v[j], sc, nm));
+        const float p1 = ex2_approx(fmaf(v[j + 1], sc, nm));
+        ps[(j >> 1) & 3] += p0 + p1;
+        const __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+        packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&pk);
       }
-      l = l * alpha + psum;  // this half's share of the row sum
-      m = m_new;
-      // P buffer free once the previous tile's P V has read it
-      wait(&p_empty, ((uint32_t)i & 1u) ^ 1u);
+      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // P buffer pb is free once the P V of two tiles back has read it
+      wait(&p_empty[pb], ((uint32_t)(i >> 1) & 1u) ^ 1u);
+      uint8_t* prow = base + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 16;
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8)
         *reinterpret_cast<uint4*>(prow + (h * 4 + c8) * 128) =
             make_uint4(packed[4 * c8], packed[4 * c8 + 1], packed[4 * c8 + 2], packed[4 * c8 + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full);
-      if (i >= 1) accumulate(i - 1, alpha_prev);
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+      // fold in the previous tile's P V (same segment)
+      if (i >= 1 && t != 0) accumulate(i - 1, alpha_prev);
+      l = l * alpha + psum;  // this half's share of the row sum
+      m = m_new;
       alpha_prev = alpha;
-    }
-    if (ntiles > 0) accumulate(ntiles - 1, alpha_prev);
-    // the row sum is split over the two halves
-    s_lsum[h][r] = l;
-    pair_bar();
-    const float lsum = l + s_lsum[h ^ 1][r];
-    if (valid) {
-      const size_t unit = ((size_t)b * A.nkv + kvh) * A.max_chunks + c;
-      float* po = A.part_o + (unit * R + r) * hd + h * 64;
+      if (i == ntiles - 1 || t == T - 1) {
+        // segment end: fold in this tile, write the unnormalised partial
+        accumulate(i, alpha_prev);
+        s_lsum[h][r] = l;
+        pair_bar();
+        const float lsum = l + s_lsum[h ^ 1][r];
+        if (valid) {
+          const long long u0 = s_tstart[b] + (long long)kvh * T;
+          int sid = s_segbase[b];
+          for (int hh = 0; hh < kvh; ++hh) {
+            const long long v0 = s_tstart[b] + (long long)hh * T;
+            sid += sp.owner(v0 + T - 1) - sp.owner(v0) + 1;
+          }
+          sid += (int)blockIdx.x - sp.owner(u0);
+          const size_t row = (size_t)sid * R + r;
+          float* po = A.part_o + row * hd + h * 64;
 #pragma unroll
-      for (int d4 = 0; d4 < 16; ++d4)
-        reinterpret_cast<float4*>(po)[d4] =
-            make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
-      if (h == 0) {
-        A.part_ml[(unit * R + r) * 2 + 0] = m;
-        A.part_ml[(unit * R + r) * 2 + 1] = lsum;
+          for (int d4 = 0; d4 < 16; ++d4)
+            reinterpret_cast<float4*>(po)[d4] =
+                make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
+          if (h == 0) {
+            A.part_ml[row * 2 + 0] = m;
+            A.part_ml[row * 2 + 1] = lsum;
+          }
+        }
+        pair_bar();  // s_lsum is reused by the next segment
       }
     }
   }
@@ -318,8 +488,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnTcArgs args) {
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, cudaStream_t st) {
-  if (A.hd != 128 || (A.nq / A.nkv) * A.W > 128 || A.Wp > kTile || A.chunk % kTile)
+// Merge the segment partials of every (sequence, row, q head): one block per
+// (b*W + p, h), one thread per head dim.  seg_table holds each unit's first
+// segment id and segment count (written by block 0 of the attention kernel).
+__global__ void attn_seg_merge_kernel(AttnArgs A) {
+  const int mh = blockIdx.x;
+  const int m = mh / A.nq, h = mh % A.nq;
+  const int b = m / A.W, p = m % A.W;
+  const int G = A.nq / A.nkv, kvh = h / G, g = h % G, R = G * A.W;
+  const int r = g * A.W + p;
+  const int u = b * A.nkv + kvh;
+  const int s0 = A.seg_table[u * 2 + 0], ns = A.seg_table[u * 2 + 1];
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, A.part_ml[((size_t)(s0 + s) * R + r) * 2]);
+  float lsum = 0.f, acc = 0.f;
+  const int d = threadIdx.x;
+  for (int s = 0; s < ns; ++s) {
+    const size_t row = (size_t)(s0 + s) * R + r;
+    const float ms = A.part_ml[row * 2];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - M);
+    lsum += A.part_ml[row * 2 + 1] * w;
+    acc += A.part_o[row * A.hd + d] * w;
+  }
+  static_cast<bf16*>(A.o)[(size_t)m * A.nq * A.hd + h * A.hd + d] =
+      __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+}
+
+cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
+                                cudaStream_t st) {
+  if (A.hd != 128 || (A.nq / A.nkv) * A.W > 128 || A.Wp > kTile || A.B > kMaxB ||
+      A.min_tiles < 1 || !A.seg_table || grid < 1)
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
@@ -328,8 +527,10 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, cudaSt
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  AttnTcArgs args{A, zero_page};
-  attn_tc_kernel<<<dim3(A.max_chunks, A.nkv, A.B), kThreads, kSmemBytes + 1024, st>>>(args);
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes + 1024, st>>>(A, zero_page);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_seg_merge_kernel<<<A.B * A.W * A.nq, A.hd, 0, st>>>(A);
   return cudaGetLastError();
 }
 

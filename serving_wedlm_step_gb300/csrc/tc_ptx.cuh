@@ -50,19 +50,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// bounded wait for the phase with the given parity to complete
+// bounded wait for the phase with the given parity to complete.  The clock
+// is read only after a first run of polls, so that ordinary handoffs never
+// pay for a timer read.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 4096; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 4096; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > kWaitNs) {
       set_err(err, WEDLM_DEV_TIMEOUT);
       return false;
     }
   }
+}
+
+// 2^x with the MUFU approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, subnormal results flushed to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ---- TMA ------------------------------------------------------------------------

@@ -10,7 +10,8 @@ import oracle as O
 from synth import (Workload, make_pool_torch, make_state_np, make_weights_torch,
                    qwen3_layers)
 from tests.gpu_common import (Stats, check_pool_writes, compare_seq, dev, pool_bits,
-                              pool_np, run_step, weights_torch_to_np, within)
+                              pool_np, run_step, teacher_forced_scores, weights_torch_to_np,
+                              within)
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -47,7 +48,9 @@ def test_one_layer_step_matches_oracle(one_layer, seed):
     assert ctx.status() == 0
     refs = O.oracle_step(s, w_np, st, ref_pools, 0.01, 1.0)
     stats = Stats()
-    compare_seq(gpu, 0, 16, refs[0], st, 0.01, 1.0, TOL, stats, s.mask_id, bf16_stored=True)
+    tf = teacher_forced_scores(gpu, 0, 16, w_np, s)
+    compare_seq(gpu, 0, 16, refs[0], st, 0.01, 1.0, TOL, stats, s.mask_id, bf16_stored=True,
+                tf=tf)
     r = refs[0]
     seqs = [(st["page_table"][0], int(st["seq_len"][0]), r.n_commit,
              r.k_win[0][r.inv[:r.n_commit]], r.v_win[0][r.inv[:r.n_commit]])]

@@ -8,7 +8,7 @@ import torch
 import oracle as O
 from synth import TINY, WORKLOADS, Workload, make_pool_np, make_state_np, make_weights_np
 from tests.gpu_common import (Stats, check_pool_writes, compare_seq, dev, pool_bits,
-                              pool_np, run_step, weights_np_to_torch)
+                              pool_np, run_step, teacher_forced_scores, weights_np_to_torch)
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -45,7 +45,8 @@ def check_step(s, wl, w_np, st, pools_np, alpha=0.01, tau=1.0, logits=True, grap
     stats = Stats()
     W = wl.window
     for b, ref in enumerate(refs):
-        compare_seq(gpu, b, W, ref, st, alpha, tau, TOL, stats, s.mask_id)
+        compare_seq(gpu, b, W, ref, st, alpha, tau, TOL, stats, s.mask_id,
+                    tf=teacher_forced_scores(gpu, b, W, w_np, s))
         if logits:
             z = gpu["logits"].numpy()[b * W:(b + 1) * W]
             fin = np.isfinite(ref.scores.logits)
@@ -143,7 +144,8 @@ def test_tiny_streaming_steps_teacher_forced():
         refs = O.oracle_step(s, w_np, state, ref_pools, 0.05, 3.0)
         stats = Stats()
         for b, ref in enumerate(refs):
-            compare_seq(gpu, b, wl.window, ref, state, 0.05, 3.0, TOL, stats, s.mask_id)
+            compare_seq(gpu, b, wl.window, ref, state, 0.05, 3.0, TOL, stats, s.mask_id,
+                        tf=teacher_forced_scores(gpu, b, wl.window, w_np, s))
             total += ref.n_commit
         after = [pool_bits(p) for p in pools]
         seqs = [(state["page_table"][b], int(state["seq_len"][b]), ref.n_commit,

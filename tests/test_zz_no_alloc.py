@@ -55,12 +55,12 @@ def test_attention_static_matches_wedlm_attention_twice():
 def test_attention_static_rejects_oversized_batch():
     from serving_wedlm_step_gb300 import binding as Bd
     from tests.gpu_common import dev
-    # 64 sequences x 8 kv heads x 64 rows x 130 floats x 4 B = 17 MB per key
-    # chunk: fewer than two chunks fit in the 32 MiB array
-    B, W = 64, 16
+    # (about 150 SMs + 16 sequences x 8 kv heads) segments x 128 rows x 130
+    # floats x 4 B is about 18.6 MB: more than the 16 MiB array
+    B, W = 16, 32
     q = torch.zeros(B * W, 32, 128, dtype=torch.bfloat16, device="cuda")
     pool = torch.zeros(2 * 2 * 8 * 16 * 128, dtype=torch.bfloat16, device="cuda")
-    win = torch.zeros(B, 2, 8, 16 * 128, dtype=torch.bfloat16, device="cuda")
+    win = torch.zeros(B, 2, 8, 32 * 128, dtype=torch.bfloat16, device="cuda")
     o = torch.zeros(B * W, 32 * 128, dtype=torch.bfloat16, device="cuda")
     pt = dev(np.zeros((B, 2), np.int32))
     sl = dev(np.zeros(B, np.int32))
