@@ -18,10 +18,12 @@
 //       they exchange only the row max of each tile.  They also stage Q at
 //       the start of each segment.  P goes to shared memory in bf16 (double
 //       buffered); O accumulates in registers with the rescale;
-//   warp 8 / lane 0: producer: a prefix tile is 4 pages of K and 4 of V
-//       (4 KiB each, already in the 8x8-tile operand layout), copied with
-//       cp.async.bulk into 4-stage K and V rings; missing or invalid pages
-//       come from a zero page; the window tile comes from the window scratch;
+//   warps 8 and 10 / lane 0: copiers of K and of V: a prefix tile is 4
+//       pages of K and 4 of V (4 KiB each, already in the 8x8-tile operand
+//       layout), copied with cp.async.bulk into 4-stage K and V rings; each
+//       ring has its own copier so that K runs ahead of the P V consumers of
+//       V; missing or invalid pages come from a zero page; the window tile
+//       comes from the window scratch;
 //   warp 9 / lane 0: MMA issuer: S = Q K^T (M = 128 query rows, N = keys,
 //       K = head_dim) into one of two TMEM score buffers, then O_tile = P V
 //       (N = head_dim; V as an MN-major operand) into one of two TMEM output
@@ -34,7 +36,7 @@ namespace wedlm {
 namespace {
 constexpr int kTile = 64;                  // keys per prefix tile (4 pages)
 constexpr int kStages = 4;
-constexpr int kThreads = 320;              // 8 softmax warps, producer, MMA
+constexpr int kThreads = 352;              // 8 softmax warps, K copier, MMA, V copier
 constexpr uint32_t kQBytes = 128 * 128 * 2;        // 128 rows x 128 dims
 constexpr uint32_t kPBytes = 128 * kTile * 2;      // 128 rows x 64 keys
 constexpr uint32_t kKVBytes = kTile * 128 * 2;     // one K or V tile
@@ -47,6 +49,7 @@ constexpr uint32_t kTmemCols = 512;  // S: 2 x 64 columns; O: 2 x 128 columns
 constexpr int kMaxB = kMaxRows;      // sequences (<= rows)
 constexpr int kPagesPerTile = kTile / kPageBlock;
 constexpr int kPrefTiles = 1024;     // tiles whose page ids are staged up front
+constexpr int kMaxGrid = 256;        // blocks of one launch
 }  // namespace
 
 // Split of the flattened tile sequence over the blocks; every block and the
@@ -55,13 +58,17 @@ struct StreamSplit {
   long long total;  // tiles of all units
   int G;            // blocks that get work
   __device__ long long begin(int c) const { return (long long)c * total / G; }
-  __device__ int owner(long long g) const {  // block holding global tile g
-    int c = (int)((g * G) / total);
-    while (c + 1 < G && begin(c + 1) <= g) ++c;
-    while (c > 0 && begin(c) > g) --c;
-    return c;
-  }
 };
+
+// largest index i in [0, n) with a[i] <= x (a ascending, a[0] <= x)
+__device__ __forceinline__ int last_le(const long long* a, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 __device__ __forceinline__ int seq_len_clamped(const AttnArgs& A, int b) {
   return max(0, min(A.seq_len[b], A.max_pages * kPageBlock));
@@ -85,9 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   __shared__ int s_issued[2], s_done[2];  // K/V tiles copied / consumed
   __shared__ float s_red[2][2][128];      // [tile parity][half][row]: row max
   __shared__ float s_lsum[2][128];        // [half][row]: segment row sums
-  __shared__ long long s_tstart[kMaxB];   // first global tile of sequence b
+  __shared__ long long s_tstart[kMaxB + 1];  // first global tile of sequence b
+  __shared__ long long s_begin[kMaxGrid + 1];  // first global tile of block c
+  __shared__ int s_T[kMaxB];                 // tiles of one unit of sequence b
   __shared__ int s_pages[kPrefTiles * kPagesPerTile];  // page ids (-1: none)
-  __shared__ int s_segbase[kMaxB];        // first segment id of sequence b
   __shared__ StreamSplit s_split;
 
   const int hd = 128, G = A.nq / A.nkv, W = A.W, R = G * W;
@@ -95,32 +103,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
-    // the plan: tiles per sequence, the block split and the segment ids
-    long long acc = 0;
-    for (int b = 0; b < A.B; ++b) {
+  // The plan, computed by the whole block: tiles per sequence, their
+  // prefix sums, the equal split of all tiles over the blocks.  A segment
+  // (the tiles of unit u inside block c) has slot u + c: along the tile
+  // order neither u nor c ever decreases and one of them grows from one
+  // segment to the next, so slots are distinct and fewer than units + G.
+  for (int b = threadIdx.x; b < A.B; b += kThreads) s_T[b] = seq_tiles(A, b);
+  __syncthreads();
+  if (warp == 0) {
+    const int per = (A.B + 31) / 32;
+    const int b0 = min(A.B, lane * per), b1 = min(A.B, b0 + per);
+    long long sum = 0;
+    for (int b = b0; b < b1; ++b) sum += (long long)s_T[b] * A.nkv;
+    long long incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    long long acc = incl - sum;
+    for (int b = b0; b < b1; ++b) {
       s_tstart[b] = acc;
-      acc += (long long)seq_tiles(A, b) * A.nkv;
+      acc += (long long)s_T[b] * A.nkv;
     }
-    StreamSplit sp;
-    sp.total = acc;
-    const long long by_min = (acc + A.min_tiles - 1) / A.min_tiles;
-    sp.G = (int)min((long long)gridDim.x, max(1LL, by_min));
-    s_split = sp;
-    int sid = 0;
-    for (int b = 0; b < A.B; ++b) {
-      s_segbase[b] = sid;
-      const int T = seq_tiles(A, b);
-      for (int h = 0; h < A.nkv; ++h) {
-        const long long u0 = s_tstart[b] + (long long)h * T;
-        const int n = sp.owner(u0 + T - 1) - sp.owner(u0) + 1;
-        if (blockIdx.x == 0) {
-          A.seg_table[(b * A.nkv + h) * 2 + 0] = sid;
-          A.seg_table[(b * A.nkv + h) * 2 + 1] = n;
-        }
-        sid += n;
-      }
+    if (lane == 31) {
+      StreamSplit sp;
+      sp.total = incl;
+      const long long by_min = (incl + A.min_tiles - 1) / A.min_tiles;
+      sp.G = (int)min((long long)min((int)gridDim.x, kMaxGrid), max(1LL, by_min));
+      s_split = sp;
+      s_tstart[A.B] = incl;
     }
+  }
+  if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
@@ -139,6 +154,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   __syncthreads();
   const StreamSplit sp = s_split;
   if ((int)blockIdx.x >= sp.G) return;  // uniform for the block
+  for (int c = threadIdx.x; c <= sp.G; c += kThreads) s_begin[c] = sp.begin(c);
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    // segment table: unit u's segments are slots u + c for the blocks c
+    // from the owner of its first tile to the owner of its last
+    for (int u = threadIdx.x; u < A.B * A.nkv; u += kThreads) {
+      const int b = u / A.nkv, h = u % A.nkv, T = s_T[b];
+      const long long u0 = s_tstart[b] + (long long)h * T;
+      const int c0 = last_le(s_begin, sp.G, u0), c1 = last_le(s_begin, sp.G, u0 + T - 1);
+      A.seg_table[u * 2 + 0] = u + c0;
+      A.seg_table[u * 2 + 1] = c1 - c0 + 1;
+    }
+  }
   if (warp == 0) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
@@ -155,17 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
     return false;
   };
 
-  const long long g0 = sp.begin(blockIdx.x);
-  const int ntiles = (int)(sp.begin(blockIdx.x + 1) - g0);
+  const long long g0 = s_begin[blockIdx.x];
+  const int ntiles = (int)(s_begin[blockIdx.x + 1] - g0);
   // position of a block tile: sequence, kv head, tile within the unit and
   // tiles of the unit; found once, then advanced tile by tile
   struct Cur { int b, kvh, t, T, L; };
   Cur first;
   {
-    first.b = 0;
-    while (first.b + 1 < A.B && s_tstart[first.b + 1] <= g0) ++first.b;
+    first.b = last_le(s_tstart, A.B, g0);
     first.L = seq_len_clamped(A, first.b);
-    first.T = (first.L + kTile - 1) / kTile + 1;
+    first.T = s_T[first.b];
     const long long off = g0 - s_tstart[first.b];
     first.kvh = (int)(off / first.T);
     first.t = (int)(off % first.T);
@@ -177,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
         c.kvh = 0;
         if (c.b + 1 < A.B) {
           c.L = seq_len_clamped(A, ++c.b);
-          c.T = (c.L + kTile - 1) / kTile + 1;
+          c.T = s_T[c.b];
         }
       }
     }
@@ -187,12 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   // every thread at once so the producer never waits on a global load
   for (int e = threadIdx.x; e < min(ntiles, kPrefTiles) * kPagesPerTile; e += kThreads) {
     const long long g = g0 + e / kPagesPerTile;
-    int b = 0, hi = A.B - 1;  // last sequence whose first tile is <= g
-    while (b < hi) {
-      const int mid = (b + hi + 1) >> 1;
-      if (s_tstart[mid] <= g) b = mid; else hi = mid - 1;
-    }
-    const int L = seq_len_clamped(A, b), T = (L + kTile - 1) / kTile + 1;
+    const int b = last_le(s_tstart, A.B, g);
+    const int L = seq_len_clamped(A, b), T = s_T[b];
     const int t = (int)((g - s_tstart[b]) % T);
     const int t0 = t * kTile + (e % kPagesPerTile) * kPageBlock;
     int pid = -1;
@@ -207,9 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   }
   __syncthreads();
 
-  if (warp == 8) {
+  if (warp == 8 || warp == 10) {
     if (lane == 0) {
-      // ---------------- producer ----------------
+      // ---------------- copiers: K (warp 8), V (warp 10) ----------------
+      const int kv = (warp == 10);
       const uint64_t pol = l2_evict_first_policy();
       const bf16* pool = static_cast<const bf16*>(A.pool);
       const bf16* win = static_cast<const bf16*>(A.kv_win);
@@ -244,27 +268,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
         const bool window = (t == T - 1);
         const int st = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        for (int kv = 0; kv < 2; ++kv) {
-          uint64_t* full = kv ? &v_full[st] : &k_full[st];
-          if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
-          uint8_t* dst = base + (kv ? kOffV : kOffK) + st * kKVBytes;
-          if (window) {
-            const uint32_t bytes = (uint32_t)A.Wp * hd * 2;
-            mbar_arrive_expect_tx(full, bytes);
-            bulk_load(dst, win + (((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp * hd, bytes, full,
-                      pol);
-          } else {
-            mbar_arrive_expect_tx(full, kKVBytes);
+        uint64_t* full = kv ? &v_full[st] : &k_full[st];
+        if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
+        uint8_t* dst = base + (kv ? kOffV : kOffK) + st * kKVBytes;
+        if (window) {
+          const uint32_t bytes = (uint32_t)A.Wp * hd * 2;
+          mbar_arrive_expect_tx(full, bytes);
+          bulk_load(dst, win + (((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp * hd, bytes, full,
+                    pol);
+        } else {
+          mbar_arrive_expect_tx(full, kKVBytes);
 #pragma unroll
-            for (int pg = 0; pg < kPg; ++pg) {
-              const void* src =
-                  pid[pg] >= 0 ? (const void*)(pool + (((size_t)pid[pg] * 2 + kv) * A.nkv + kvh) * blockn)
-                               : zero_page;
-              bulk_load(dst + pg * kPageBytes, src, kPageBytes, full, pol);
-            }
+          for (int pg = 0; pg < kPg; ++pg) {
+            const void* src =
+                pid[pg] >= 0
+                    ? (const void*)(pool + (((size_t)pid[pg] * 2 + kv) * A.nkv + kvh) * blockn)
+                    : zero_page;
+            bulk_load(dst + pg * kPageBytes, src, kPageBytes, full, pol);
           }
-          s_issued[kv] = i + 1;
         }
+        s_issued[kv] = i + 1;
       }
     }
   } else if (warp == 9) {
@@ -452,14 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
         pair_bar();
         const float lsum = l + s_lsum[h ^ 1][r];
         if (valid) {
-          const long long u0 = s_tstart[b] + (long long)kvh * T;
-          int sid = s_segbase[b];
-          for (int hh = 0; hh < kvh; ++hh) {
-            const long long v0 = s_tstart[b] + (long long)hh * T;
-            sid += sp.owner(v0 + T - 1) - sp.owner(v0) + 1;
-          }
-          sid += (int)blockIdx.x - sp.owner(u0);
-          const size_t row = (size_t)sid * R + r;
+          const size_t sid = (size_t)b * A.nkv + kvh + blockIdx.x;
+          const size_t row = sid * R + r;
           float* po = A.part_o + row * hd + h * 64;
 #pragma unroll
           for (int d4 = 0; d4 < 16; ++d4)
@@ -527,7 +544,7 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes + 1024, st>>>(A, zero_page);
+  attn_tc_kernel<<<min(grid, kMaxGrid), kThreads, kSmemBytes + 1024, st>>>(A, zero_page);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_seg_merge_kernel<<<A.B * A.W * A.nq, A.hd, 0, st>>>(A);
