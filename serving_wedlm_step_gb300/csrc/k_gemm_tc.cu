@@ -16,8 +16,8 @@
 //   warps 2-5: epilogue, one activation row per thread (TMEM lane quadrant
 //       = warp % 4), straight from TMEM (epilogue_tc.cuh), overlapping the
 //       next unit's mainloop.  With split-K they store the fp32 partial;
-//       splitk_epilogue_kernel then sums the partials in split order and
-//       runs the epilogue with one thread per (row, epilogue item).
+//       a split-K epilogue kernel then sums the partials in split order,
+//       consecutive threads on consecutive columns, and runs the epilogue.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -226,9 +226,114 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   if (warp == 2) tmem_dealloc(tmem, L.tmem_cols);
 }
 
-// Split-K: sum the partials of every split in split order (deterministic)
-// and run the epilogue.  Grid (tiles * items, row blocks of 128); thread =
-// (activation row, epilogue item).
+// Split-K epilogues.  The partial sums of every split are added in split
+// order (deterministic), with consecutive threads on consecutive columns so
+// that every partial is read once, coalesced.
+
+// sum of the splits at float4 index i of [M][N]
+__device__ __forceinline__ float4 splitk_sum4(const GemmProblem& P, size_t i) {
+  const float4* p4 = reinterpret_cast<const float4*>(P.partial);
+  const size_t stride4 = (size_t)P.M * P.N / 4;
+  float4 a = __ldcg(p4 + i);
+  for (int sp = 1; sp < P.splits; ++sp) {
+    const float4 t = __ldcg(p4 + sp * stride4 + i);
+    a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
+  }
+  return a;
+}
+
+// RESID: x[m][n] += acc[m][n]
+__global__ void __launch_bounds__(256) splitk_resid_kernel(GemmProblem P) {
+  const size_t n4 = (size_t)P.M * P.N / 4;
+  bf16* x = static_cast<bf16*>(P.epi.x);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = splitk_sum4(P, i);
+    __nv_bfloat162* xp = reinterpret_cast<__nv_bfloat162*>(x + 4 * i);
+    const float2 x01 = __bfloat1622float2(xp[0]), x23 = __bfloat1622float2(xp[1]);
+    xp[0] = __floats2bfloat162_rn(x01.x + a.x, x01.y + a.y);
+    xp[1] = __floats2bfloat162_rn(x23.x + a.z, x23.y + a.w);
+  }
+}
+
+// SWIGLU: act[m][f] = silu(gate) * up; tile t holds gate features
+// [t*half, (t+1)*half) in columns [0, half) and the same up features in
+// [half, ntile)
+__global__ void __launch_bounds__(256) splitk_swiglu_kernel(GemmProblem P, int ntile) {
+  const int half = ntile / 2, F = P.N / 2;
+  const size_t n4 = (size_t)P.M * F / 4;
+  bf16* act = static_cast<bf16*>(P.epi.act);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = 4 * i;
+    const int m = (int)(e / F), f = (int)(e % F);
+    const int t = f / half, c = f % half;
+    const size_t g4 = ((size_t)m * P.N + (size_t)t * ntile + c) / 4;
+    const float4 g = splitk_sum4(P, g4), u = splitk_sum4(P, g4 + half / 4);
+    const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
+    float o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = gv[k] / (1.0f + expf(-gv[k])) * uv[k];
+    __nv_bfloat162* ap = reinterpret_cast<__nv_bfloat162*>(act + e);
+    ap[0] = __floats2bfloat162_rn(o[0], o[1]);
+    ap[1] = __floats2bfloat162_rn(o[2], o[3]);
+  }
+}
+
+// QKV (head_dim 128): one warp per (row, head), lane l holds dims 4l..4l+3.
+// q and k heads: per-head RMSNorm (when enabled), then RoPE on the pairs
+// (d, d + 64), which sit in lanes l and l ^ 16; q goes to q_out, k and v
+// to the layer's window scratch in the 8x8-tile layout.
+__global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
+  const GemmEpi& e = P.epi;
+  const int lane = threadIdx.x & 31;
+  const int heads = P.N / 128;
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= P.M * heads) return;
+  const int m = wid / heads, gh = wid % heads;
+  const int kind = gh < e.nq ? 0 : (gh < e.nq + e.nkv ? 1 : 2);
+  const float4 a = splitk_sum4(P, ((size_t)m * P.N + (size_t)gh * 128) / 4 + lane);
+  float x[4] = {a.x, a.y, a.z, a.w};
+  const int d0 = 4 * lane;
+  if (kind < 2) {
+    if (e.qk_norm) {
+      float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+      ss = warp_sum(ss);
+      const float rs = rsqrtf(ss / 128.f + e.eps);
+      const bf16* gw = static_cast<const bf16*>(kind == 0 ? e.q_norm : e.k_norm) + d0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = x[k] * rs * __bfloat162float(gw[k]);
+    }
+    float y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = __shfl_xor_sync(0xffffffffu, x[k], 16);
+    const int dh = d0 & 63;  // position within the rotated half
+    const float4 c4 = *reinterpret_cast<const float4*>(e.cosb + (size_t)m * 64 + dh);
+    const float4 s4 = *reinterpret_cast<const float4*>(e.sinb + (size_t)m * 64 + dh);
+    const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+    if (lane < 16) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = x[k] * cs[k] - y[k] * sn[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = x[k] * cs[k] + y[k] * sn[k];
+    }
+  }
+  bf16* dst;
+  if (kind == 0) {
+    dst = static_cast<bf16*>(e.q_out) + ((size_t)m * e.nq + gh) * 128 + d0;
+  } else {
+    const int b = m / e.W, p = m % e.W;
+    const int kvh = gh - e.nq - (kind == 2 ? e.nkv : 0);
+    dst = static_cast<bf16*>(e.kv_win) + (((size_t)b * 2 + (kind - 1)) * e.nkv + kvh) * e.Wp * 128 +
+          tile_off(p, d0, 128);
+  }
+  __nv_bfloat162* dp = reinterpret_cast<__nv_bfloat162*>(dst);
+  dp[0] = __floats2bfloat162_rn(x[0], x[1]);
+  dp[1] = __floats2bfloat162_rn(x[2], x[3]);
+}
+
+// any other epilogue: thread = (activation row, epilogue item)
 __global__ void __launch_bounds__(128)
 splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
   const int tile = blockIdx.x / items, item = blockIdx.x % items;
@@ -389,8 +494,21 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   if (P.splits > 1) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int items = tc_epi_items(P, L.ntile);
-    splitk_epilogue_kernel<<<dim3(L.tiles * items, L.nrb), 128, 0, st>>>(P, L.ntile, items);
+    const int cap = plans.num_sms * 8;  // grid-stride beyond 8 blocks per SM
+    if (P.epi.mode == EPI_RESID) {
+      const size_t n4 = (size_t)P.M * P.N / 4;
+      splitk_resid_kernel<<<(int)std::min<size_t>((n4 + 255) / 256, cap), 256, 0, st>>>(P);
+    } else if (P.epi.mode == EPI_SWIGLU) {
+      const size_t n4 = (size_t)P.M * (P.N / 2) / 4;
+      splitk_swiglu_kernel<<<(int)std::min<size_t>((n4 + 255) / 256, cap), 256, 0, st>>>(
+          P, L.ntile);
+    } else if (P.epi.mode == EPI_QKV && P.epi.hd == 128) {
+      const int warps = P.M * (P.N / 128);
+      splitk_qkv_kernel<<<(warps + 7) / 8, 256, 0, st>>>(P);
+    } else {
+      const int items = tc_epi_items(P, L.ntile);
+      splitk_epilogue_kernel<<<dim3(L.tiles * items, L.nrb), 128, 0, st>>>(P, L.ntile, items);
+    }
   }
   return cudaGetLastError();
 }
