@@ -1,56 +1,81 @@
 // Paged causal GQA window attention on the 5th-generation tensor cores.
 //
-// The step is "a small causal prefill over the active window on top of
-// cached KV" (WeDLM summary page, Key claims §5.2): the G*W query rows of
-// one kv head (G = nq/nkv q heads x W window rows, physical order) attend to
-// every cached prefix position and, causally, to the window (§3.2).
+// In a WeDLM decode step the window is attended to like a short causal
+// prefill on top of the cached prefix (WeDLM summary page, Key claims §5.2):
+// the G*W query rows of one kv head (G = nq/nkv q heads x W window rows,
+// physical order) attend to every cached prefix position and, causally, to
+// the window (§3.2).
 //
-// Work = unit (sequence b, kv head) x 64-key tiles: ceil(L_b/64) prefix
+// Work = unit (sequence b, kv head) x 128-key tiles: ceil(L_b/128) prefix
 // tiles, then one window tile.  Stream-K: the units' tiles are laid end to
 // end and every block (one per SM) takes an equal contiguous share, so a
-// block processes runs ("segments") of consecutive tiles of one unit; O, the
-// running max and the sum stay in registers across a segment and each
-// segment writes one unnormalised partial, combined by attn_seg_merge_kernel.
-// Warp roles:
-//   warps 0-7: online softmax.  Warps q and q+4 share TMEM lane quadrant q
-//       (query rows 32q..32q+31, thread = row): warp q takes key columns
-//       0-31 of each tile and head dims 0-63 of O, warp q+4 the other halves;
-//       they exchange only the row max of each tile.  They also stage Q at
-//       the start of each segment.  P goes to shared memory in bf16 (double
-//       buffered); O accumulates in registers with the rescale;
-//   warps 8 and 10 / lane 0: copiers of K and of V: a prefix tile is 4
-//       pages of K and 4 of V (4 KiB each, already in the 8x8-tile operand
-//       layout), copied with cp.async.bulk into 4-stage K and V rings; each
-//       ring has its own copier so that K runs ahead of the P V consumers of
-//       V; missing or invalid pages come from a zero page; the window tile
-//       comes from the window scratch;
-//   warp 9 / lane 0: MMA issuer: S = Q K^T (M = 128 query rows, N = keys,
-//       K = head_dim) into one of two TMEM score buffers, then O_tile = P V
-//       (N = head_dim; V as an MN-major operand) into one of two TMEM output
-//       buffers.
+// block processes runs ("segments") of consecutive tiles of one unit; each
+// segment writes one unnormalised partial (O, running max, row sum) and
+// attn_seg_merge_kernel combines them.
+//
+// Row r of a unit is (window row p, q head g) with r = p*G + g: the order in
+// which one TMA box {8 dims, G heads, W tokens} of q lands in shared memory.
+//
+// Data path of one tile i (everything the softmax warps and the MMA issuer
+// hand each other lives in TMEM):
+//   S_i = Q K_i^T   (tcgen05.mma, M = 128 query rows, N = 128 keys, K = 128
+//                    dims; A = Q, B = K_i from shared memory) -> TMEM S[i&1]
+//   P_i = 2^(S_i * scale - m)   (softmax warps, bf16)        -> TMEM P[i&1]
+//   O  += P_i V_i   (tcgen05.mma with A = P_i read from TMEM, B = V_i from
+//                    shared memory, N = 128 dims)             -> TMEM O
+// The running max m of a row is raised only when a tile's max exceeds it by
+// more than 2^8; then O (once the previous P V is done) and the row sum are
+// rescaled.  Between raises the exponentials are taken against the stale
+// max, which is exact after the final division because O and the row sum
+// share it, and keeps every P value below 2^8.
+//
+// Warp roles (352 threads):
+//   warps 0-7: softmax.  Warps q and q+4 share TMEM lane quadrant q (query
+//       rows 32q..32q+31, thread = row): warp q takes keys 0-63 of each tile
+//       and head dims 0-63 of O, warp q+4 the other halves; they exchange
+//       the row max of each tile through shared memory;
+//   warp 8 / lane 0: K copier: Q of each segment (16 TMA boxes into one of
+//       two Q buffers) and the K tiles (8 pages of 4 KiB, already in the
+//       8x8-tile operand layout, by cp.async.bulk) into the K ring;
+//   warp 9 / lane 0: MMA issuer;
+//   warp 10 / lane 0: V copier: the V tiles into the V ring.
+// Missing or invalid pages come from a zero page; the window tile comes from
+// the window scratch.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
 namespace wedlm {
 
 namespace {
-constexpr int kTile = 64;                  // keys per prefix tile (4 pages)
-constexpr int kStages = 4;
-constexpr int kThreads = 352;              // 8 softmax warps, K copier, MMA, V copier
-constexpr uint32_t kQBytes = 128 * 128 * 2;        // 128 rows x 128 dims
-constexpr uint32_t kPBytes = 128 * kTile * 2;      // 128 rows x 64 keys
-constexpr uint32_t kKVBytes = kTile * 128 * 2;     // one K or V tile
-constexpr uint32_t kOffP = kQBytes;
-constexpr uint32_t kOffK = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-constexpr uint32_t kSmemBytes = kOffV + kStages * kKVBytes;   // 192 KB
-constexpr uint32_t kPageBytes = 16 * 128 * 2;                 // 4 KiB
-constexpr uint32_t kTmemCols = 512;  // S: 2 x 64 columns; O: 2 x 128 columns
-constexpr int kMaxB = kMaxRows;      // sequences (<= rows)
+constexpr int kTile = 128;                 // keys per prefix tile (8 pages)
 constexpr int kPagesPerTile = kTile / kPageBlock;
-constexpr int kPrefTiles = 1024;     // tiles whose page ids are staged up front
-constexpr int kMaxGrid = 256;        // blocks of one launch
+constexpr int kMaxStages = 4;              // per ring
+constexpr int kThreads = 352;
+constexpr uint32_t kKVBytes = kTile * 128 * 2;         // one K or V tile: 32 KiB
+constexpr uint32_t kPageBytes = kPageBlock * 128 * 2;  // 4 KiB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;      // S[0], S[1]: 128 fp32 columns each
+constexpr uint32_t kColO = 256;    // O: 128 fp32 columns
+constexpr uint32_t kColP = 384;    // P[0], P[1]: 64 columns each (bf16 pairs)
+constexpr float kRescaleLog2 = 8.f;        // raise the running max beyond 2^8
+constexpr int kMaxB = kMaxRows;            // sequences (<= rows)
+constexpr int kPrefTiles = 256;            // tiles whose page ids are staged
+constexpr int kMaxGrid = 256;              // blocks of one launch
+constexpr uint32_t kDynBytes = 205 * 1024; // dynamic shared memory (+1 KiB align)
 }  // namespace
+
+// ring depths and shared-memory carve-up of one launch (host-chosen)
+struct AttnLayout {
+  int R, Rpad;          // rows of a unit, rounded up to 8
+  int KS, VS;           // K and V ring depths
+  uint32_t q_bytes;     // one Q buffer: 16 dim groups x Rpad rows x 16 B
+  uint32_t off_k, off_v;
+};
 
 // Split of the flattened tile sequence over the blocks; every block and the
 // segment table agree on it.
@@ -81,24 +106,66 @@ __device__ __forceinline__ uint32_t idesc_pv() {  // M=128, N=128, B MN-major
   return idesc_bf16_m128(128) | (1u << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const void* zero_page) {
+// 3-D tiled TMA load (tensor map in kernel-parameter space)
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16; A (M x K) is read from
+// TMEM: lane = row, each 32-bit column holds two consecutive K elements
+// (the lower K index in the low half)
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns from registers into TMEM
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly,
+               const void* zero_page) {
   extern __shared__ uint8_t dsm_raw[];
-  __shared__ __align__(8) uint64_t k_full[kStages], k_empty[kStages];
-  __shared__ __align__(8) uint64_t v_full[kStages], v_empty[kStages];
-  __shared__ __align__(8) uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  __shared__ __align__(8) uint64_t p_full[2], p_empty[2], q_full, q_empty;
+  __shared__ __align__(8) uint64_t k_full[kMaxStages], k_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t v_full[kMaxStages], v_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
+  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], p_empty[2], o_free;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_issued[2], s_done[2];  // K/V tiles copied / consumed
+  __shared__ int s_issued[3], s_done[3];  // K, V, Q copies issued / consumed
   __shared__ float s_red[2][2][128];      // [tile parity][half][row]: row max
   __shared__ float s_lsum[2][128];        // [half][row]: segment row sums
-  __shared__ long long s_tstart[kMaxB + 1];  // first global tile of sequence b
+  __shared__ long long s_tstart[kMaxB + 1];    // first global tile of sequence b
   __shared__ long long s_begin[kMaxGrid + 1];  // first global tile of block c
-  __shared__ int s_T[kMaxB];                 // tiles of one unit of sequence b
+  __shared__ int s_T[kMaxB];                   // tiles of one unit of sequence b
   __shared__ int s_pages[kPrefTiles * kPagesPerTile];  // page ids (-1: none)
   __shared__ StreamSplit s_split;
 
-  const int hd = 128, G = A.nq / A.nkv, W = A.W, R = G * W;
+  const int hd = 128, G = A.nq / A.nkv, W = A.W, R = Ly.R;
+  const int KS = Ly.KS, VS = Ly.VS;
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,19 +203,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
     }
   }
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 8);
-      mbar_init(&o_full[i], 1); mbar_init(&o_free[i], 8);
       mbar_init(&p_full[i], 8); mbar_init(&p_empty[i], 1);
     }
-    mbar_init(&q_full, 8);
-    mbar_init(&q_empty, 1);
+    mbar_init(&o_free, 8);
     s_abort = 0;
-    s_issued[0] = s_issued[1] = s_done[0] = s_done[1] = 0;
+    for (int k = 0; k < 3; ++k) s_issued[k] = s_done[k] = 0;
     mbar_fence_init();
   }
   __syncthreads();
@@ -211,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   };
 
   // page ids of the block's first kPrefTiles tiles, loaded and checked by
-  // every thread at once so the producer never waits on a global load
+  // every thread at once so the copiers never wait on a global load
   for (int e = threadIdx.x; e < min(ntiles, kPrefTiles) * kPagesPerTile; e += kThreads) {
     const long long g = g0 + e / kPagesPerTile;
     const int b = last_le(s_tstart, A.B, g);
@@ -232,25 +298,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
 
   if (warp == 8 || warp == 10) {
     if (lane == 0) {
-      // ---------------- copiers: K (warp 8), V (warp 10) ----------------
+      // ---------------- copiers: K (+ Q) (warp 8), V (warp 10) ----------------
       const int kv = (warp == 10);
+      const int NS = kv ? VS : KS;
       const uint64_t pol = l2_evict_first_policy();
       const bf16* pool = static_cast<const bf16*>(A.pool);
       const bf16* win = static_cast<const bf16*>(A.kv_win);
       const size_t blockn = (size_t)kPageBlock * hd;
       constexpr int kPg = kPagesPerTile;
-      // page ids of a tile (-1: no page there): staged in shared memory for
-      // the first kPrefTiles tiles, loaded directly beyond that
-      auto tile_pages = [&](int i, const Cur& c, int (&pid)[kPg]) {
+      if (!kv) tma_prefetch_desc(&mq);
+      int seg = -1;
+      Cur cur = first;
+      for (int i = 0; i < ntiles; ++i, advance(cur)) {
+        const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
+        if (!kv && (i == 0 || t == 0)) {
+          // a new segment: its Q into buffer seg & 1, once the S MMAs of the
+          // segment two back are done with it
+          ++seg;
+          const int qb = seg & 1;
+          if (!wait(&q_empty[qb], ((uint32_t)(seg >> 1) & 1u) ^ 1u)) break;
+          uint8_t* qdst = base + qb * Ly.q_bytes;
+          mbar_arrive_expect_tx(&q_full[qb], (uint32_t)(16 * R * 16));
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c)
+            tma_load_3d(qdst + c * Ly.Rpad * 16, &mq, &q_full[qb], 8 * c, kvh * G, b * W);
+          s_issued[2] = seg + 1;
+        }
+        int pid[kPg];
 #pragma unroll
         for (int pg = 0; pg < kPg; ++pg) {
           if (i < kPrefTiles) {
             pid[pg] = s_pages[i * kPg + pg];
           } else {
-            const int t0 = c.t * kTile + pg * kPageBlock;
+            const int t0 = t * kTile + pg * kPageBlock;
             int v = -1;
-            if (c.t != c.T - 1 && t0 < c.L) {
-              v = A.page_table[(size_t)c.b * A.max_pages + t0 / kPageBlock];
+            if (t != T - 1 && t0 < cur.L) {
+              v = A.page_table[(size_t)b * A.max_pages + t0 / kPageBlock];
               if (v < 0 || v >= A.num_pages) {
                 set_err(A.err, WEDLM_DEV_BAD_PAGE);
                 v = -1;
@@ -259,19 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
             pid[pg] = v;
           }
         }
-      };
-      Cur cur = first;
-      for (int i = 0; i < ntiles; ++i, advance(cur)) {
-        int pid[kPg];
-        tile_pages(i, cur, pid);
-        const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
-        const bool window = (t == T - 1);
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        const int st = i % NS;
+        const uint32_t ph = (uint32_t)(i / NS) & 1u;
         uint64_t* full = kv ? &v_full[st] : &k_full[st];
         if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
-        uint8_t* dst = base + (kv ? kOffV : kOffK) + st * kKVBytes;
-        if (window) {
+        uint8_t* dst = base + (kv ? Ly.off_v : Ly.off_k) + st * kKVBytes;
+        if (t == T - 1) {
           const uint32_t bytes = (uint32_t)A.Wp * hd * 2;
           mbar_arrive_expect_tx(full, bytes);
           bulk_load(dst, win + (((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp * hd, bytes, full,
@@ -293,118 +369,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   } else if (warp == 9) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t sq = smem_u32(base);
       const uint32_t idPV = idesc_pv();
-      int seg = -1;  // segment counter (Q buffer phases)
-      Cur cs = first;  // position of the next S to issue
+      const uint32_t qlbo = (uint32_t)Ly.Rpad * 16;  // next 8-dim group of Q
+      int seg_s = -1, seg_o = -1;
+      Cur cs = first, cp = first;  // positions of the next S and the next P V
       auto issue_s = [&](int i) -> bool {
         const int t = cs.t, T = cs.T;
         advance(cs);
-        if (i == 0 || t == 0) {  // a new segment: wait for its Q
-          ++seg;
-          if (!wait(&q_full, (uint32_t)seg & 1u)) return false;
+        const bool seg_first = (i == 0 || t == 0), seg_last = (i == ntiles - 1 || t == T - 1);
+        if (seg_first) {
+          ++seg_s;
+          if (!wait(&q_full[seg_s & 1], (uint32_t)(seg_s >> 1) & 1u)) return false;
+          s_done[2] = seg_s + 1;
         }
-        const int st = i % kStages, sb = i & 1;
-        if (!wait(&k_full[st], (uint32_t)(i / kStages) & 1u)) return false;
+        const int st = i % KS, sb = i & 1;
+        if (!wait(&k_full[st], (uint32_t)(i / KS) & 1u)) return false;
         s_done[0] = i + 1;
         if (!wait(&s_free[sb], ((uint32_t)(i >> 1) & 1u) ^ 1u)) return false;
         tc_fence_after();
-        const uint32_t sk = smem_u32(base + kOffK + st * kKVBytes);
+        const uint32_t sq = smem_u32(base + (seg_s & 1) * Ly.q_bytes);
+        const uint32_t sk = smem_u32(base + Ly.off_k + st * kKVBytes);
         const uint32_t idS = idesc_bf16_m128(t == T - 1 ? A.Wp : kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem + (uint32_t)(sb * 64), sdesc_noswz(sq + kk * 256, 128, 2048),
+        for (int kk = 0; kk < 8; ++kk)  // 16 dims a step: two 8-dim groups
+          tc_mma_f16(tmem + kColS + (uint32_t)(sb * 128),
+                     sdesc_noswz(sq + kk * 2 * qlbo, qlbo, 128),
                      sdesc_noswz(sk + kk * 256, 128, 2048), idS, kk ? 1u : 0u);
         tc_commit(&s_full[sb]);
         tc_commit(&k_empty[st]);
-        if (i == ntiles - 1 || t == T - 1) tc_commit(&q_empty);  // segment's last S
+        if (seg_last) tc_commit(&q_empty[seg_s & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int i) -> bool {
+        const int t = cp.t, T = cp.T;
+        advance(cp);
+        const bool seg_first = (i == 0 || t == 0);
+        const int st = i % VS, pb = i & 1;
+        if (!wait(&v_full[st], (uint32_t)(i / VS) & 1u)) return false;
+        s_done[1] = i + 1;
+        if (!wait(&p_full[pb], (uint32_t)(i >> 1) & 1u)) return false;
+        if (seg_first) {
+          // O is overwritten: the previous segment's O must have been read
+          ++seg_o;
+          if (seg_o > 0 && !wait(&o_free, (uint32_t)(seg_o - 1) & 1u)) return false;
+        }
+        tc_fence_after();
+        const uint32_t sv = smem_u32(base + Ly.off_v + st * kKVBytes);
+        const int nk = (t == T - 1) ? A.Wp : kTile;
+        for (int kk = 0; kk < nk / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
+          tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(pb * 64 + kk * 8),
+                        sdesc_noswz(sv + kk * 4096, 2048, 128), idPV,
+                        (seg_first && kk == 0) ? 0u : 1u);
+        tc_commit(&p_empty[pb]);
+        tc_commit(&v_empty[st]);
         return true;
       };
       bool ok = issue_s(0);
-      Cur cur = first;
-      for (int i = 0; i < ntiles && ok; ++i, advance(cur)) {
-        const int t = cur.t, T = cur.T;
-        // within a segment the next S goes ahead of this P V; across a
-        // segment boundary it must wait for the next Q, which the softmax
-        // warps stage only after this tile's P V
-        const bool next_same = (i + 1 < ntiles) && (t != T - 1);
-        if (next_same && !issue_s(i + 1)) break;
-        const int st = i % kStages, ob = i & 1, pb = i & 1;
-        if (!wait(&v_full[st], (uint32_t)(i / kStages) & 1u)) break;
-        s_done[1] = i + 1;
-        if (!wait(&p_full[pb], (uint32_t)(i >> 1) & 1u)) break;
-        if (!wait(&o_free[ob], ((uint32_t)(i >> 1) & 1u) ^ 1u)) break;
-        tc_fence_after();
-        const uint32_t sv = smem_u32(base + kOffV + st * kKVBytes);
-        const uint32_t spp = smem_u32(base + kOffP + pb * kPBytes);
-        const int nk = (t == T - 1) ? A.Wp : kTile;
-        for (int kk = 0; kk < nk / 16; ++kk)
-          tc_mma_f16(tmem + 128u + (uint32_t)(ob * 128), sdesc_noswz(spp + kk * 256, 128, 1024),
-                     sdesc_noswz(sv + kk * 4096, 2048, 128), idPV, kk ? 1u : 0u);
-        tc_commit(&o_full[ob]);
-        tc_commit(&v_empty[st]);
-        tc_commit(&p_empty[pb]);
-        if (i + 1 < ntiles && !next_same && !issue_s(i + 1)) break;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (i + 1 < ntiles && !issue_s(i + 1)) break;
+        ok = issue_pv(i);
       }
     }
   } else {
     // ---------------- softmax warps ----------------
-    const int q = warp & 3, h = warp >> 2;       // lane quadrant, column / dim half
+    const int q = warp & 3, h = warp >> 2;       // lane quadrant, key / dim half
     const int r = 32 * q + lane;                  // query row
     const bool valid = r < R;
-    const int p_row = valid ? r % W : 0;
+    const int p_row = valid ? r / G : 0;          // window row of this query row
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     const float sc = A.scale_log2;
-    const int tid = threadIdx.x;                  // 0..255
-    float o[64];
-#pragma unroll
-    for (int d = 0; d < 64; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
-    int seg = -1;
+    float m = -INFINITY, l = 0.f;
     auto pair_bar = [&]() {  // warps q and q+4
       asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
-    };
-    auto softmax_bar = [&]() {  // the 8 softmax warps
-      asm volatile("bar.sync 5, 256;" ::: "memory");
-    };
-    auto accumulate = [&](int i, float alpha) {
-      const int ob = i & 1;
-      wait(&o_full[ob], (uint32_t)(i >> 1) & 1u);
-      tc_fence_after();
-#pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        float v[32];
-        tmem_ld32(trow + 128u + (uint32_t)(ob * 128 + h * 64 + cb * 32), v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[cb * 32 + j] = fmaf(o[cb * 32 + j], alpha, v[j]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[ob]);
     };
     Cur cur = first;
     for (int i = 0; i < ntiles; ++i, advance(cur)) {
       const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
-      if (i == 0 || t == 0) {
-        // new segment: stage its Q once the previous segment's S MMAs are done
-        ++seg;
-        wait(&q_empty, ((uint32_t)seg & 1u) ^ 1u);
-        const bf16* qg = static_cast<const bf16*>(A.q);
-        for (int idx = tid; idx < 128 * 16; idx += 256) {
-          const int rr = idx >> 4, d8 = idx & 15;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (rr < R) {
-            const int g = rr / W, p = rr % W;
-            v = *reinterpret_cast<const uint4*>(
-                qg + ((size_t)(b * W + p) * A.nq + kvh * G + g) * hd + d8 * 8);
-          }
-          *reinterpret_cast<uint4*>(base + (rr >> 3) * 2048 + d8 * 128 + (rr & 7) * 16) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        softmax_bar();
-        if (lane == 0) mbar_arrive(&q_full);
-#pragma unroll
-        for (int d = 0; d < 64; ++d) o[d] = 0.f;
+      const bool seg_first = (i == 0 || t == 0), seg_last = (i == ntiles - 1 || t == T - 1);
+      if (seg_first) {
         m = -INFINITY;
         l = 0.f;
       }
@@ -413,8 +455,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
       const int sb = i & 1, pb = i & 1;
       wait(&s_full[sb], (uint32_t)(i >> 1) & 1u);
       tc_fence_after();
-      float v[32];
-      tmem_ld32(trow + (uint32_t)(sb * 64 + h * 32), v);
+      float v[64];
+      {
+        float a[32], c[32];
+        tmem_ld32(trow + kColS + (uint32_t)(sb * 128 + h * 64), a);
+        tmem_ld32(trow + kColS + (uint32_t)(sb * 128 + h * 64 + 32), c);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) { v[j] = a[j]; v[32 + j] = c[j]; }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
@@ -423,29 +471,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
       const int kbase = t * kTile;
       if (window || kbase + kTile > L) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int jj = h * 32 + j;
+        for (int j = 0; j < 64; ++j) {
+          const int jj = h * 64 + j;
           const bool ok = window ? (jj < W && jj <= p_row) : (kbase + jj < L);
           if (!ok) v[j] = -INFINITY;
         }
       }
       float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mx[k] = fmaxf(fmaxf(v[4 * k], v[4 * k + 1]), fmaxf(v[4 * k + 2], v[4 * k + 3]));
+      for (int k = 0; k < 8; ++k) {
+        mx[k] = fmaxf(fmaxf(v[8 * k], v[8 * k + 1]), fmaxf(v[8 * k + 2], v[8 * k + 3]));
+        mx[k] = fmaxf(mx[k], fmaxf(fmaxf(v[8 * k + 4], v[8 * k + 5]),
+                                   fmaxf(v[8 * k + 6], v[8 * k + 7])));
+      }
       const float hmax =
           fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
       s_red[i & 1][h][r] = hmax;
       pair_bar();
-      const float m_new = fmaxf(m, fmaxf(hmax, s_red[i & 1][h ^ 1][r]));
-      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-      // p = 2^(s*scale - m_new); masked scores are -inf and give 0
-      const float nm = (m_new == -INFINITY) ? 0.f : -m_new;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t packed[16];
+      const float m_tile = fmaxf(hmax, s_red[i & 1][h ^ 1][r]);
+      // both halves take the same decision for a row (same m_tile, same
+      // history); the TMEM loads and stores below are warp-collective, so a
+      // warp enters when any of its rows raises and the other rows scale by 1
+      const bool raise = m_tile > m + kRescaleLog2;
+      if (__any_sync(0xffffffffu, raise)) {
+        const float alpha = !raise ? 1.f : (m == -INFINITY) ? 0.f : ex2_approx(m - m_tile);
+        if (!seg_first) {
+          // O holds this segment's earlier tiles: wait for the last P V
+          // (tile i-1) and scale this thread's half row of O in TMEM
+          wait(&p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u);
+          tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
+          for (int cb = 0; cb < 2; ++cb) {
+            float o[32];
+            uint32_t u[32];
+            const uint32_t ta = trow + kColO + (uint32_t)(h * 64 + cb * 32);
+            tmem_ld32(ta, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(o[j] * alpha);
+            tmem_st32(ta, u);
+          }
+          tmem_wait_st();
+        }
+        if (raise) {
+          l *= alpha;
+          m = m_tile;
+        }
+      }
+      // p = 2^(s*scale - m); masked scores are -inf and give 0
+      const float nm = (m == -INFINITY) ? 0.f : -m;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t packed[32];
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) {
         const float p0 = ex2_approx(fmaf(v[j], sc, nm));
         const float p1 = ex2_approx(fmaf(v[j + 1], sc, nm));
         ps[(j >> 1) & 3] += p0 + p1;
@@ -453,24 +531,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
         packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&pk);
       }
       const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P buffer pb is free once the P V of two tiles back has read it
+      // P buffer pb is free once the P V of two tiles back is done
       wait(&p_empty[pb], ((uint32_t)(i >> 1) & 1u) ^ 1u);
-      uint8_t* prow = base + kOffP + pb * kPBytes + (r >> 3) * 1024 + (r & 7) * 16;
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8)
-        *reinterpret_cast<uint4*>(prow + (h * 4 + c8) * 128) =
-            make_uint4(packed[4 * c8], packed[4 * c8 + 1], packed[4 * c8 + 2], packed[4 * c8 + 3]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_after();
+      tmem_st32(trow + kColP + (uint32_t)(pb * 64 + h * 32), packed);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
-      // fold in the previous tile's P V (same segment)
-      if (i >= 1 && t != 0) accumulate(i - 1, alpha_prev);
-      l = l * alpha + psum;  // this half's share of the row sum
-      m = m_new;
-      alpha_prev = alpha;
-      if (i == ntiles - 1 || t == T - 1) {
-        // segment end: fold in this tile, write the unnormalised partial
-        accumulate(i, alpha_prev);
+      l += psum;  // this half's share of the row sum
+      if (seg_last) {
+        // segment end: once this tile's P V is done, read O and write the
+        // unnormalised partial
+        wait(&p_empty[pb], (uint32_t)(i >> 1) & 1u);
+        tc_fence_after();
+        float o[64];
+        {
+          float a[32], c[32];
+          tmem_ld32(trow + kColO + (uint32_t)(h * 64), a);
+          tmem_ld32(trow + kColO + (uint32_t)(h * 64 + 32), c);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = c[j]; }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free);
         s_lsum[h][r] = l;
         pair_bar();
         const float lsum = l + s_lsum[h ^ 1][r];
@@ -496,58 +581,109 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs A, const 
   tc_fence_after();
   if (s_abort && threadIdx.x == 256) {
     // after a timeout: wait (bounded) for this block's copies still in flight
-    for (int kv = 0; kv < 2; ++kv)
+    for (int kv = 0; kv < 2; ++kv) {
+      const int NS = kv ? VS : KS;
       for (int i = s_done[kv]; i < s_issued[kv]; ++i)
-        mbar_wait(kv ? &v_full[i % kStages] : &k_full[i % kStages],
-                  (uint32_t)(i / kStages) & 1u, A.err);
+        mbar_wait(kv ? &v_full[i % NS] : &k_full[i % NS], (uint32_t)(i / NS) & 1u, A.err);
+    }
+    for (int s = s_done[2]; s < s_issued[2]; ++s)
+      mbar_wait(&q_full[s & 1], (uint32_t)(s >> 1) & 1u, A.err);
   }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge the segment partials of every (sequence, row, q head): one block per
-// (b*W + p, h), one thread per head dim.  seg_table holds each unit's first
-// segment id and segment count (written by block 0 of the attention kernel).
-__global__ void attn_seg_merge_kernel(AttnArgs A) {
-  const int mh = blockIdx.x;
-  const int m = mh / A.nq, h = mh % A.nq;
+// Merge the segment partials of every (window row, q head): one warp each,
+// lane = 4 head dims.  seg_table holds each unit's first segment slot and
+// segment count (written by block 0 of the attention kernel).
+__global__ void __launch_bounds__(256) attn_seg_merge_kernel(AttnArgs A) {
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (wid >= A.B * A.W * A.nq) return;
+  const int m = wid / A.nq, h = wid % A.nq;
   const int b = m / A.W, p = m % A.W;
   const int G = A.nq / A.nkv, kvh = h / G, g = h % G, R = G * A.W;
-  const int r = g * A.W + p;
+  const int r = p * G + g;
   const int u = b * A.nkv + kvh;
   const int s0 = A.seg_table[u * 2 + 0], ns = A.seg_table[u * 2 + 1];
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, A.part_ml[((size_t)(s0 + s) * R + r) * 2]);
-  float lsum = 0.f, acc = 0.f;
-  const int d = threadIdx.x;
+  float lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < ns; ++s) {
     const size_t row = (size_t)(s0 + s) * R + r;
     const float ms = A.part_ml[row * 2];
     if (ms == -INFINITY) continue;
     const float w = exp2f(ms - M);
     lsum += A.part_ml[row * 2 + 1] * w;
-    acc += A.part_o[row * A.hd + d] * w;
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(A.part_o + row * A.hd) + lane);
+    acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
   }
-  static_cast<bf16*>(A.o)[(size_t)m * A.nq * A.hd + h * A.hd + d] =
-      __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  __nv_bfloat162* dst =
+      reinterpret_cast<__nv_bfloat162*>(static_cast<bf16*>(A.o) + ((size_t)m * A.nq + h) * A.hd) +
+      2 * lane;
+  dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
 }
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 attn_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
 
 cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
                                 cudaStream_t st) {
-  if (A.hd != 128 || (A.nq / A.nkv) * A.W > 128 || A.Wp > kTile || A.B > kMaxB ||
-      A.min_tiles < 1 || !A.seg_table || grid < 1)
+  const int G = A.nq / A.nkv;
+  if (A.hd != 128 || G * A.W > 128 || A.Wp > 64 || A.B > kMaxB || A.min_tiles < 1 ||
+      !A.seg_table || grid < 1 || (reinterpret_cast<uintptr_t>(A.q) & 15))
+    return cudaErrorInvalidValue;
+  AttnLayout Ly;
+  Ly.R = G * A.W;
+  Ly.Rpad = (Ly.R + 7) / 8 * 8;
+  Ly.q_bytes = 256u * (uint32_t)Ly.Rpad;
+  const int stages = (int)((kDynBytes - 2 * Ly.q_bytes) / kKVBytes);
+  Ly.KS = stages >= 6 ? 3 : 2;
+  Ly.VS = std::min(kMaxStages, stages - Ly.KS);
+  if (Ly.VS < 2) return cudaErrorInvalidValue;
+  Ly.off_k = 2 * Ly.q_bytes;
+  Ly.off_v = Ly.off_k + (uint32_t)Ly.KS * kKVBytes;
+  // q as a 3-D tensor {dim, head, token}; a box {8, G, W} is one 8-dim
+  // group of the G*W rows of one unit
+  auto enc = attn_encoder();
+  if (!enc) return cudaErrorInvalidValue;
+  CUtensorMap mq;
+  cuuint64_t dims[3] = {128, (cuuint64_t)A.nq, (cuuint64_t)A.B * A.W};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)A.nq * 128 * 2};
+  cuuint32_t box[3] = {8, (cuuint32_t)G, (cuuint32_t)A.W};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A.q), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(
-        attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes + 1024);
+        attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes + 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_tc_kernel<<<min(grid, kMaxGrid), kThreads, kSmemBytes + 1024, st>>>(A, zero_page);
+  const uint32_t smem = Ly.off_v + (uint32_t)Ly.VS * kKVBytes + 1024;
+  attn_tc_kernel<<<std::min(grid, kMaxGrid), kThreads, smem, st>>>(mq, A, Ly, zero_page);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_seg_merge_kernel<<<A.B * A.W * A.nq, A.hd, 0, st>>>(A);
+  const int warps = A.B * A.W * A.nq;
+  attn_seg_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(A);
   return cudaGetLastError();
 }
 

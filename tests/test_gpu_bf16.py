@@ -109,6 +109,48 @@ def test_ragged_attention_matches_oracle():
     assert worst <= TOL
 
 
+def test_growing_scores_attention_matches_oracle():
+    """Keys scaled up page by page (factor 1 + j/4 on logical page j), so the
+    row maxima keep growing along the prefix and different query rows raise
+    their running max on different tiles of a segment."""
+    s = qwen3_layers(1)
+    wl = Workload("growing", s, batch=8, window=16, prefix=(4000, 8192), masked=(4, 12),
+                  shuffled_pages=True, seed=3)
+    st = make_state_np(wl)
+    B, W, nq, nkv, hd = 8, 16, s.n_q_heads, s.n_kv_heads, s.head_dim
+    pool = make_pool_torch(s, st["num_pages"], 0, 0)
+    scale = torch.ones(st["num_pages"], dtype=torch.float32)
+    for b in range(B):
+        n_pages = (int(st["seq_len"][b]) + 15) // 16
+        for j in range(n_pages):
+            scale[int(st["page_table"][b][j])] = 1.0 + 0.25 * j
+    k_view = pool.view(st["num_pages"], 2, -1)[:, 0]  # K of every page: [page][nkv*16*hd]
+    k_view.copy_((k_view.float() * scale.cuda().view(-1, 1)).to(torch.bfloat16))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    q = torch.randn(B * W, nq, hd, generator=g, device="cuda").to(torch.bfloat16)
+    kw = torch.randn(B, W, nkv, hd, generator=g, device="cuda").to(torch.bfloat16)
+    vw = torch.randn(B, W, nkv, hd, generator=g, device="cuda").to(torch.bfloat16)
+    kw_np, vw_np = kw.float().cpu().numpy(), vw.float().cpu().numpy()
+    win = dev(_pack_window(kw_np, vw_np, 16), torch.bfloat16)
+    w = make_weights_torch(s, seed=0)
+    ctx = _ctx(s, w, W, B, st["max_pages"])
+    o = torch.empty(B * W, nq * hd, dtype=torch.bfloat16, device="cuda")
+    ctx.attention(q, pool, dev(st["page_table"]), dev(st["seq_len"]), st["num_pages"], win, o)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    o_np = o.float().cpu().numpy().reshape(B, W, nq, hd)
+    q_np = q.float().cpu().numpy().reshape(B, W, nq, hd)
+    pool_f = pool_np(pool)
+    worst = 0.0
+    for b in range(B):
+        kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
+        ref = O.window_attention(q_np[b], kp, vp, kw_np[b], vw_np[b])
+        worst = max(worst, float(np.abs(o_np[b] - ref).max()))
+    print("growing-scores attention max err", worst)
+    assert worst <= TOL
+
+
 def test_ragged_layer_matches_oracle(one_layer):
     """The whole decoder layer at the ragged shape (B=32, 512 window rows),
     sampled sequences compared with the oracle layer on the same input."""
