@@ -50,7 +50,7 @@ struct wedlm_ctx {
   size_t win_layer_stride = 0;  // elements
   float *attn_o = nullptr, *attn_ml = nullptr;
   int attn_chunk = 0, attn_max_chunks = 0;
-  int* attn_seg_table = nullptr;  // tensor-core attention: [B*nkv][2]
+  int* attn_unit_cnt = nullptr;   // tensor-core attention: [B*nkv] segment counts
   float* gemm_part = nullptr;
   size_t gemm_part_elems = 0;
   int* gemm_counters = nullptr;
@@ -179,7 +179,7 @@ cudaError_t run_attention<float>(wedlm_ctx*, const AttnArgs& A, cudaStream_t st)
 }
 template <>
 cudaError_t run_attention<bf16>(wedlm_ctx* c, const AttnArgs& A, cudaStream_t st) {
-  return launch_attention_tc(A, c->zero_page, c->num_sms, st);  // attention + merge
+  return launch_attention_tc(A, c->zero_page, c->num_sms, st);
 }
 
 AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
@@ -195,22 +195,30 @@ AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
   A.kv_win = kv_win; A.part_o = c->attn_o; A.part_ml = c->attn_ml; A.o = o;
   A.err = c->err;
   A.min_tiles = 2;
-  A.seg_table = c->attn_seg_table;
+  A.unit_cnt = c->attn_unit_cnt;
   return A;
 }
 
-// rows a2..a4 for one layer, on workspace activations
+// rows a2..a4 for one layer, on workspace activations.  xn_ready: xn
+// already holds RMSNorm(x) with this layer's attention norm (written by the
+// previous layer's down projection); next_norm: when set, the down
+// projection's epilogue also writes xn = RMSNorm(x) with these weights (the
+// next layer's attention norm or the final norm).  Both are used on the
+// tensor-core path only, where the residual epilogue can fuse the norm.
 template <typename T>
 int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
                const int32_t* page_table, int num_pages, const void* pool,
-               void* kv_win_layer, cudaStream_t st) {
+               void* kv_win_layer, cudaStream_t st, bool xn_ready = false,
+               const void* next_norm = nullptr) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
   const int M = B * g.window, H = g.hidden, hd = g.head_dim;
   const int nq = g.n_q_heads, nkv = g.n_kv_heads;
+  const bool fuse = g.dtype == WEDLM_BF16;
   int rc;
-  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
-         launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
+  if (!xn_ready)
+    LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+           launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
   {
     GemmProblem P{};
     P.M = M; P.N = (nq + 2 * nkv) * hd; P.K = H; P.X = c->xn;
@@ -226,9 +234,8 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
   AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
                          kv_win_layer, c->o);
   if (g.dtype == WEDLM_BF16) {
-    // tensor-core attention and its segment merge: two kernels
+    // tensor-core attention: one kernel (the segment merge is inside)
     LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
-    c->launch_count += 1;
   } else {
     LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
     LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
@@ -238,10 +245,14 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
     P.M = M; P.N = H; P.K = nq * hd; P.X = c->o;
     P.A0 = w.w_o; P.A1 = w.w_o; P.A2 = w.w_o; P.seg1 = H; P.seg2 = H;
     P.epi.mode = EPI_RESID; P.epi.x = x;
+    if (fuse) {  // residual add + the FFN norm in one epilogue
+      P.epi.norm_w = w.ffn_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
+    }
     if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_O, st))) return rc;
   }
-  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
-         launch_rmsnorm<T>(M, H, x, (const T*)w.ffn_norm, g.rms_eps, (T*)c->xn, st));
+  if (!fuse)
+    LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+           launch_rmsnorm<T>(M, H, x, (const T*)w.ffn_norm, g.rms_eps, (T*)c->xn, st));
   {
     GemmProblem P{};
     P.M = M; P.N = 2 * g.ffn; P.K = H; P.X = c->xn;
@@ -255,20 +266,25 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
     P.M = M; P.N = H; P.K = g.ffn; P.X = c->act;
     P.A0 = w.w_down; P.A1 = w.w_down; P.A2 = w.w_down; P.seg1 = H; P.seg2 = H;
     P.epi.mode = EPI_RESID; P.epi.x = x;
+    if (fuse && next_norm) {
+      P.epi.norm_w = next_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
+    }
     if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_DOWN, st))) return rc;
   }
   return WEDLM_OK;
 }
 
+// xn_ready: xn already holds RMSNorm(x) with the final norm
 template <typename T>
 int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant_phys,
-                float plant_bias, float* logits, cudaStream_t st) {
+                float plant_bias, float* logits, cudaStream_t st, bool xn_ready = false) {
   const wedlm_config& g = c->cfg;
   const int M = B * g.window;
   int rc;
-  LAUNCH(c, WEDLM_KIND_RMSNORM, st,
-         launch_rmsnorm<T>(M, g.hidden, x, (const T*)c->final_norm, g.rms_eps,
-                           (T*)c->xn, st));
+  if (!xn_ready)
+    LAUNCH(c, WEDLM_KIND_RMSNORM, st,
+           launch_rmsnorm<T>(M, g.hidden, x, (const T*)c->final_norm, g.rms_eps,
+                             (T*)c->xn, st));
   GemmProblem P{};
   P.M = M; P.N = g.vocab; P.K = g.hidden; P.X = c->xn;
   P.A0 = c->lm_head; P.A1 = c->lm_head; P.A2 = c->lm_head;
@@ -320,15 +336,21 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
                                  c->perm, c->inv, c->pos_phys, c->seq_snap,
                                  c->plant_phys, (T*)c->x, c->cosb, c->sinb,
                                  c->err, st));
+  // on the tensor-core path each down projection also normalises x for
+  // the next layer (or the LM head)
+  const bool fuse = g.dtype == WEDLM_BF16;
   for (int l = 0; l < g.n_layers; ++l) {
     void* win = (char*)c->kv_win + (size_t)l * c->win_layer_stride * c->es;
+    const void* next_norm =
+        !fuse ? nullptr : (l + 1 < g.n_layers ? c->layers[l + 1].attn_norm : c->final_norm);
     if ((rc = layer_impl<T>(c, l, B, (T*)c->x, c->seq_snap, in->page_table,
-                            in->num_pages, in->kv_pools[l], win, st)))
+                            in->num_pages, in->kv_pools[l], win, st, fuse && l > 0,
+                            next_norm)))
       return rc;
   }
   if ((rc = lmhead_impl<T>(c, B, (const T*)c->x,
                            in->plant_token ? c->plant_phys : nullptr,
-                           in->plant_bias, out->logits, st)))
+                           in->plant_bias, out->logits, st, fuse)))
     return rc;
   SelArgs S{};
   S.B = B; S.W = W; S.mask_id = g.mask_id; S.alpha = in->alpha; S.tau = in->tau;
@@ -475,7 +497,7 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   const size_t slots = std::max(units * C->attn_max_chunks, (size_t)C->num_sms + units);
   WA(C->attn_o, slots * R * hd * 4);
   WA(C->attn_ml, slots * R * 2 * 4);
-  WA(C->attn_seg_table, units * 2 * 4);
+  WA(C->attn_unit_cnt, units * 4);
   WA(C->gemm_part, C->gemm_part_elems * 4);
   WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
   WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
@@ -535,6 +557,10 @@ int wedlm_get_status(wedlm_ctx* c, int32_t* device_error) {
   int32_t word = 0;
   CUDA_TRY(c, cudaMemcpy(&word, c->err, 4, cudaMemcpyDeviceToHost));
   CUDA_TRY(c, cudaMemset(c->err, 0, 4));
+  // a launch that gave up on a wait may have left segment counts behind
+  if (word)
+    CUDA_TRY(c, cudaMemset(c->attn_unit_cnt, 0,
+                           (size_t)c->cfg.max_batch * c->cfg.n_kv_heads * 4));
   if (device_error) *device_error = word;
   if (word) return fail(c, WEDLM_ERR_DEVICE, "device error word " + std::to_string(word));
   return WEDLM_OK;

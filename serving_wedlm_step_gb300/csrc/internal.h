@@ -11,12 +11,18 @@
 
 namespace wedlm {
 
+// threads of one RMSNorm block (one block per row); the fused residual +
+// norm epilogue uses the same count so that both reduce in the same order
+constexpr int kNormThreads = 512;
+
 enum EpiMode { EPI_RESID = 0, EPI_SWIGLU = 1, EPI_QKV = 2, EPI_LMHEAD = 3 };
 
 // Epilogue of the weight-streaming GEMM Y[m][n] = sum_k X[m][k] W[n][k].
 struct GemmEpi {
   int mode;
   void* x;              // RESID: residual stream [M][N], updated in place
+  const void* norm_w;   // RESID (tensor-core path): when set, also write
+  void* xn;             //   xn = RMSNorm(x) * norm_w (eps below) for the next GEMM
   void* act;            // SWIGLU: out [M][N/2] = silu(gate) * up
   // QKV
   void* q_out;          // [M][nq*hd]
@@ -67,7 +73,8 @@ struct AttnArgs {
   int* err;
   // tensor-core (stream-K) attention: partials per segment
   int min_tiles;        // fewest 64-key tiles a block is given
-  int* seg_table;       // [B*nkv][2]: first segment id, segment count
+  int* unit_cnt;        // [B*nkv]: segments of each unit written so far (zero
+                        // between launches; the unit's merging block resets it)
 };
 
 struct LayerWeights {

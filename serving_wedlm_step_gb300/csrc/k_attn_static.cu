@@ -69,9 +69,9 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms < 1)
     return WEDLM_ERR_CUDA;
-  // segment table + partials of at most (blocks + units) segments of R rows
+  // segment counts + partials of at most (blocks + units) segments of R rows
   const size_t units = (size_t)batch * n_kv_heads;
-  const size_t table_bytes = ((units * 2 * sizeof(int) + 255) / 256) * 256;
+  const size_t table_bytes = ((units * sizeof(int) + 255) / 256) * 256;
   const size_t slots = (size_t)sms + units;
   const size_t need = kPartOff + table_bytes + slots * R * (hd + 2) * sizeof(float);
   if (need > kAttnStaticScratchBytes) return WEDLM_ERR_CAPACITY;  // beyond the array
@@ -81,7 +81,10 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch + kErrOff, 0, 4, st) != cudaSuccess) return WEDLM_ERR_CUDA;
-  int* seg_table = reinterpret_cast<int*>(scratch + kPartOff);
+  int* unit_cnt = reinterpret_cast<int*>(scratch + kPartOff);
+  // the kernel leaves the counts at zero; clearing them here as well keeps a
+  // call that gave up on a wait from leaking counts into the next one
+  if (cudaMemsetAsync(unit_cnt, 0, units * sizeof(int), st) != cudaSuccess) return WEDLM_ERR_CUDA;
   float* part_o = reinterpret_cast<float*>(scratch + kPartOff + table_bytes);
   float* part_ml = part_o + slots * R * hd;
 
@@ -93,7 +96,7 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
   A.kv_win = kv_win; A.part_o = part_o; A.part_ml = part_ml; A.o = o;
   A.err = reinterpret_cast<int*>(scratch + kErrOff);
   A.min_tiles = 2;
-  A.seg_table = seg_table;
+  A.unit_cnt = unit_cnt;
   if (launch_attention_tc(A, scratch + kZeroOff, sms, st) != cudaSuccess) return WEDLM_ERR_CUDA;
   return WEDLM_OK;
 }

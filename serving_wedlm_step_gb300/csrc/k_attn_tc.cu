@@ -9,27 +9,31 @@
 // Work = unit (sequence b, kv head) x 128-key tiles: ceil(L_b/128) prefix
 // tiles, then one window tile.  Stream-K: the units' tiles are laid end to
 // end and every block (one per SM) takes an equal contiguous share, so a
-// block processes runs ("segments") of consecutive tiles of one unit; each
-// segment writes one unnormalised partial (O, running max, row sum) and
-// attn_seg_merge_kernel combines them.
+// block processes runs ("segments") of consecutive tiles of one unit.  A
+// unit inside one block is normalised and written out directly; otherwise
+// each segment writes an unnormalised partial (O, running max, row sum) and
+// the block that finishes a unit's last segment (a per-unit counter) merges
+// the partials and writes the output.
 //
 // Row r of a unit is (window row p, q head g) with r = p*G + g: the order in
 // which one TMA box {8 dims, G heads, W tokens} of q lands in shared memory.
 //
-// Data path of one tile i (everything the softmax warps and the MMA issuer
+// Data path of one tile i (everything the softmax warps and the MMA issuers
 // hand each other lives in TMEM):
 //   S_i = Q K_i^T   (tcgen05.mma, M = 128 query rows, N = 128 keys, K = 128
-//                    dims; A = Q, B = K_i from shared memory) -> TMEM S[i&1]
-//   P_i = 2^(S_i * scale - m)   (softmax warps, bf16)        -> TMEM P[i&1]
+//                    dims; A = Q, B = K_i from shared memory) -> TMEM S[i%3]
+//   P_i = 2^(S_i * scale - m)   (softmax warps, bf16, written over the first
+//                    64 columns of S[i%3])
 //   O  += P_i V_i   (tcgen05.mma with A = P_i read from TMEM, B = V_i from
 //                    shared memory, N = 128 dims)             -> TMEM O
+// S buffer i%3 is free again once P_i V_i is done.
 // The running max m of a row is raised only when a tile's max exceeds it by
 // more than 2^8; then O (once the previous P V is done) and the row sum are
 // rescaled.  Between raises the exponentials are taken against the stale
 // max, which is exact after the final division because O and the row sum
 // share it, and keeps every P value below 2^8.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-7: softmax.  Warps q and q+4 share TMEM lane quadrant q (query
 //       rows 32q..32q+31, thread = row): warp q takes keys 0-63 of each tile
 //       and head dims 0-63 of O, warp q+4 the other halves; they exchange
@@ -37,8 +41,11 @@
 //   warp 8 / lane 0: K copier: Q of each segment (16 TMA boxes into one of
 //       two Q buffers) and the K tiles (8 pages of 4 KiB, already in the
 //       8x8-tile operand layout, by cp.async.bulk) into the K ring;
-//   warp 9 / lane 0: MMA issuer;
-//   warp 10 / lane 0: V copier: the V tiles into the V ring.
+//   warp 9 / lane 0: S issuer (S = Q K^T);
+//   warp 10 / lane 0: V copier: the V tiles into the V ring;
+//   warp 11 / lane 0: P V issuer.  Each issuer's commits track only its own
+//       MMAs; S and P V touch disjoint TMEM columns, so the two streams run
+//       independently and neither waits behind the other's operands.
 // Missing or invalid pages come from a zero page; the window tile comes from
 // the window scratch.
 #include <cudaTypedefs.h>
@@ -55,13 +62,13 @@ namespace {
 constexpr int kTile = 128;                 // keys per prefix tile (8 pages)
 constexpr int kPagesPerTile = kTile / kPageBlock;
 constexpr int kMaxStages = 4;              // per ring
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr uint32_t kKVBytes = kTile * 128 * 2;         // one K or V tile: 32 KiB
 constexpr uint32_t kPageBytes = kPageBlock * 128 * 2;  // 4 KiB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S[0], S[1]: 128 fp32 columns each
-constexpr uint32_t kColO = 256;    // O: 128 fp32 columns
-constexpr uint32_t kColP = 384;    // P[0], P[1]: 64 columns each (bf16 pairs)
+constexpr uint32_t kColS = 0;      // S[0..2]: 128 fp32 columns each; P over the first 64
+constexpr uint32_t kColO = 384;    // O: 128 fp32 columns
+constexpr int kSBuf = 3;
 constexpr float kRescaleLog2 = 8.f;        // raise the running max beyond 2^8
 constexpr int kMaxB = kMaxRows;            // sequences (<= rows)
 constexpr int kPrefTiles = 256;            // tiles whose page ids are staged
@@ -144,6 +151,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// 32 lanes x 64 consecutive fp32 columns of TMEM into 64 registers per thread
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, "
+      "[%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+        "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+        "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+        "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly,
@@ -152,9 +186,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   __shared__ __align__(8) uint64_t k_full[kMaxStages], k_empty[kMaxStages];
   __shared__ __align__(8) uint64_t v_full[kMaxStages], v_empty[kMaxStages];
   __shared__ __align__(8) uint64_t q_full[2], q_empty[2];
-  __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full[2], p_empty[2], o_free;
+  __shared__ __align__(8) uint64_t s_full[kSBuf], s_free[kSBuf], p_full[kSBuf], o_free;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
+  __shared__ int s_abort, s_merge;
   __shared__ int s_issued[3], s_done[3];  // K, V, Q copies issued / consumed
   __shared__ float s_red[2][2][128];      // [tile parity][half][row]: row max
   __shared__ float s_lsum[2][128];        // [half][row]: segment row sums
@@ -209,8 +243,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
-      mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 8);
-      mbar_init(&p_full[i], 8); mbar_init(&p_empty[i], 1);
+    }
+    for (int i = 0; i < kSBuf; ++i) {
+      mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 1); mbar_init(&p_full[i], 8);
     }
     mbar_init(&o_free, 8);
     s_abort = 0;
@@ -222,17 +257,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   if ((int)blockIdx.x >= sp.G) return;  // uniform for the block
   for (int c = threadIdx.x; c <= sp.G; c += kThreads) s_begin[c] = sp.begin(c);
   __syncthreads();
-  if (blockIdx.x == 0) {
-    // segment table: unit u's segments are slots u + c for the blocks c
-    // from the owner of its first tile to the owner of its last
-    for (int u = threadIdx.x; u < A.B * A.nkv; u += kThreads) {
-      const int b = u / A.nkv, h = u % A.nkv, T = s_T[b];
-      const long long u0 = s_tstart[b] + (long long)h * T;
-      const int c0 = last_le(s_begin, sp.G, u0), c1 = last_le(s_begin, sp.G, u0 + T - 1);
-      A.seg_table[u * 2 + 0] = u + c0;
-      A.seg_table[u * 2 + 1] = c1 - c0 + 1;
-    }
-  }
   if (warp == 0) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
@@ -368,66 +392,70 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t idPV = idesc_pv();
+      // ---------------- S issuer ----------------
       const uint32_t qlbo = (uint32_t)Ly.Rpad * 16;  // next 8-dim group of Q
-      int seg_s = -1, seg_o = -1;
-      Cur cs = first, cp = first;  // positions of the next S and the next P V
-      auto issue_s = [&](int i) -> bool {
+      const uint64_t dq0 = sdesc_noswz(smem_u32(base), qlbo, 128);
+      const uint64_t dq1 = sdesc_noswz(smem_u32(base + Ly.q_bytes), qlbo, 128);
+      const uint64_t dk0 = sdesc_noswz(smem_u32(base + Ly.off_k), 128, 2048);
+      const uint64_t dq_step = (uint64_t)((2 * qlbo) >> 4);  // 16 dims, in 16-byte units
+      int seg = -1;
+      Cur cs = first;
+      for (int i = 0; i < ntiles; ++i, advance(cs)) {
         const int t = cs.t, T = cs.T;
-        advance(cs);
         const bool seg_first = (i == 0 || t == 0), seg_last = (i == ntiles - 1 || t == T - 1);
         if (seg_first) {
-          ++seg_s;
-          if (!wait(&q_full[seg_s & 1], (uint32_t)(seg_s >> 1) & 1u)) return false;
-          s_done[2] = seg_s + 1;
+          ++seg;
+          if (!wait(&q_full[seg & 1], (uint32_t)(seg >> 1) & 1u)) break;
+          s_done[2] = seg + 1;
         }
-        const int st = i % KS, sb = i & 1;
-        if (!wait(&k_full[st], (uint32_t)(i / KS) & 1u)) return false;
+        const int st = i % KS, sb = i % kSBuf;
+        if (!wait(&k_full[st], (uint32_t)(i / KS) & 1u)) break;
         s_done[0] = i + 1;
-        if (!wait(&s_free[sb], ((uint32_t)(i >> 1) & 1u) ^ 1u)) return false;
+        // S buffer sb is free once P V of tile i - 3 is done
+        if (!wait(&s_free[sb], ((uint32_t)(i / kSBuf) & 1u) ^ 1u)) break;
         tc_fence_after();
-        const uint32_t sq = smem_u32(base + (seg_s & 1) * Ly.q_bytes);
-        const uint32_t sk = smem_u32(base + Ly.off_k + st * kKVBytes);
+        const uint64_t aq = (seg & 1) ? dq1 : dq0;
+        const uint64_t bk = dk0 + (uint64_t)((st * kKVBytes) >> 4);
         const uint32_t idS = idesc_bf16_m128(t == T - 1 ? A.Wp : kTile);
+        const uint32_t dS = tmem + kColS + (uint32_t)(sb * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // 16 dims a step: two 8-dim groups
-          tc_mma_f16(tmem + kColS + (uint32_t)(sb * 128),
-                     sdesc_noswz(sq + kk * 2 * qlbo, qlbo, 128),
-                     sdesc_noswz(sk + kk * 256, 128, 2048), idS, kk ? 1u : 0u);
+          tc_mma_f16(dS, aq + kk * dq_step, bk + (uint64_t)(kk * 16), idS, kk ? 1u : 0u);
         tc_commit(&s_full[sb]);
         tc_commit(&k_empty[st]);
-        if (seg_last) tc_commit(&q_empty[seg_s & 1]);
-        return true;
-      };
-      auto issue_pv = [&](int i) -> bool {
+        if (seg_last) tc_commit(&q_empty[seg & 1]);
+      }
+    }
+  } else if (warp == 11) {
+    if (lane == 0) {
+      // ---------------- P V issuer ----------------
+      const uint32_t idPV = idesc_pv();
+      const uint64_t dv0 = sdesc_noswz(smem_u32(base + Ly.off_v), 2048, 128);
+      int seg = -1;
+      Cur cp = first;
+      for (int i = 0; i < ntiles; ++i, advance(cp)) {
         const int t = cp.t, T = cp.T;
-        advance(cp);
         const bool seg_first = (i == 0 || t == 0);
-        const int st = i % VS, pb = i & 1;
-        if (!wait(&v_full[st], (uint32_t)(i / VS) & 1u)) return false;
+        const int st = i % VS, pb = i % kSBuf;
+        if (!wait(&v_full[st], (uint32_t)(i / VS) & 1u)) break;
         s_done[1] = i + 1;
-        if (!wait(&p_full[pb], (uint32_t)(i >> 1) & 1u)) return false;
+        if (!wait(&p_full[pb], (uint32_t)(i / kSBuf) & 1u)) break;
         if (seg_first) {
           // O is overwritten: the previous segment's O must have been read
-          ++seg_o;
-          if (seg_o > 0 && !wait(&o_free, (uint32_t)(seg_o - 1) & 1u)) return false;
+          ++seg;
+          if (seg > 0 && !wait(&o_free, (uint32_t)(seg - 1) & 1u)) break;
         }
         tc_fence_after();
-        const uint32_t sv = smem_u32(base + Ly.off_v + st * kKVBytes);
-        const int nk = (t == T - 1) ? A.Wp : kTile;
-        for (int kk = 0; kk < nk / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
-          tc_mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)(pb * 64 + kk * 8),
-                        sdesc_noswz(sv + kk * 4096, 2048, 128), idPV,
-                        (seg_first && kk == 0) ? 0u : 1u);
-        tc_commit(&p_empty[pb]);
+        const uint64_t bv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
+        const uint32_t ap = tmem + kColS + (uint32_t)(pb * 128);
+        const int steps = ((t == T - 1) ? A.Wp : kTile) / 16;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
+          if (kk < steps)
+            tc_mma_f16_ts(tmem + kColO, ap + (uint32_t)(kk * 8), bv + (uint64_t)(kk * 256),
+                          idPV, (seg_first && kk == 0) ? 0u : 1u);
+        tc_commit(&s_free[pb]);
         tc_commit(&v_empty[st]);
-        return true;
-      };
-      bool ok = issue_s(0);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        if (i + 1 < ntiles && !issue_s(i + 1)) break;
-        ok = issue_pv(i);
       }
     }
   } else {
@@ -442,6 +470,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     auto pair_bar = [&]() {  // warps q and q+4
       asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
     };
+    auto softmax_bar = [&]() {  // the 8 softmax warps
+      asm volatile("bar.sync 5, 256;" ::: "memory");
+    };
     Cur cur = first;
     for (int i = 0; i < ntiles; ++i, advance(cur)) {
       const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
@@ -452,20 +483,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       }
       const bool window = (t == T - 1);
       const int L = cur.L;
-      const int sb = i & 1, pb = i & 1;
-      wait(&s_full[sb], (uint32_t)(i >> 1) & 1u);
+      const int sb = i % kSBuf;
+      const uint32_t sph = (uint32_t)(i / kSBuf) & 1u;  // phase of this tile on buffer sb
+      wait(&s_full[sb], sph);
       tc_fence_after();
       float v[64];
-      {
-        float a[32], c[32];
-        tmem_ld32(trow + kColS + (uint32_t)(sb * 128 + h * 64), a);
-        tmem_ld32(trow + kColS + (uint32_t)(sb * 128 + h * 64 + 32), c);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) { v[j] = a[j]; v[32 + j] = c[j]; }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      tmem_ld64(trow + kColS + (uint32_t)(sb * 128 + h * 64), v);
       // mask (only the partial last prefix tile and the window tile need
       // one), row max over both halves of the tile, scale applied once
       const int kbase = t * kTile;
@@ -499,7 +522,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         if (!seg_first) {
           // O holds this segment's earlier tiles: wait for the last P V
           // (tile i-1) and scale this thread's half row of O in TMEM
-          wait(&p_empty[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u);
+          wait(&s_free[(i - 1) % kSBuf], (uint32_t)((i - 1) / kSBuf) & 1u);
           tc_fence_after();
 #pragma unroll
           for (int cb = 0; cb < 2; ++cb) {
@@ -531,45 +554,143 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&pk);
       }
       const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P buffer pb is free once the P V of two tiles back is done
-      wait(&p_empty[pb], ((uint32_t)(i >> 1) & 1u) ^ 1u);
-      tc_fence_after();
-      tmem_st32(trow + kColP + (uint32_t)(pb * 64 + h * 32), packed);
+      // P over the first 64 columns of S: both halves have read their S
+      // columns before the row-max exchange above
+      tmem_st32(trow + kColS + (uint32_t)(sb * 128 + h * 32), packed);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
       l += psum;  // this half's share of the row sum
       if (seg_last) {
         // segment end: once this tile's P V is done, read O and write the
         // unnormalised partial
-        wait(&p_empty[pb], (uint32_t)(i >> 1) & 1u);
+        wait(&s_free[sb], sph);
         tc_fence_after();
         float o[64];
-        {
-          float a[32], c[32];
-          tmem_ld32(trow + kColO + (uint32_t)(h * 64), a);
-          tmem_ld32(trow + kColO + (uint32_t)(h * 64 + 32), c);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) { o[j] = a[j]; o[32 + j] = c[j]; }
-        }
+        tmem_ld64(trow + kColO + (uint32_t)(h * 64), o);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free);
         s_lsum[h][r] = l;
         pair_bar();
         const float lsum = l + s_lsum[h ^ 1][r];
-        if (valid) {
-          const size_t sid = (size_t)b * A.nkv + kvh + blockIdx.x;
-          const size_t row = sid * R + r;
-          float* po = A.part_o + row * hd + h * 64;
+        // the unit's segments: slots u + c for the blocks c from the owner
+        // of its first tile to the owner of its last
+        const int u = b * A.nkv + kvh;
+        const long long u0 = s_tstart[b] + (long long)kvh * T;
+        const int c0 = last_le(s_begin, sp.G, u0), c1 = last_le(s_begin, sp.G, u0 + T - 1);
+        if (c0 == c1) {
+          // the whole unit is in this block: normalise and write the output
+          if (valid) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            bf16* dst = static_cast<bf16*>(A.o) +
+                        ((size_t)(b * W + p_row) * A.nq + kvh * G + r % G) * hd + h * 64;
 #pragma unroll
-          for (int d4 = 0; d4 < 16; ++d4)
-            reinterpret_cast<float4*>(po)[d4] =
-                make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
-          if (h == 0) {
-            A.part_ml[row * 2 + 0] = m;
-            A.part_ml[row * 2 + 1] = lsum;
+            for (int j8 = 0; j8 < 8; ++j8) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat162 t2 =
+                    __floats2bfloat162_rn(o[8 * j8 + 2 * k] * inv, o[8 * j8 + 2 * k + 1] * inv);
+                w4[k] = *reinterpret_cast<const uint32_t*>(&t2);
+              }
+              reinterpret_cast<uint4*>(dst)[j8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        } else {
+          if (valid) {
+            // partial O as [slot][half][dim/4][row] float4s: a warp's rows
+            // are consecutive, so every store is one contiguous 512 bytes
+            const size_t sid = (size_t)u + blockIdx.x, row = sid * R + r;
+            float4* po = reinterpret_cast<float4*>(A.part_o) + (sid * 2 + h) * 16 * R + r;
+#pragma unroll
+            for (int d4 = 0; d4 < 16; ++d4)
+              po[(size_t)d4 * R] =
+                  make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
+            if (h == 0) {
+              A.part_ml[row * 2 + 0] = m;
+              A.part_ml[row * 2 + 1] = lsum;
+            }
+          }
+          __threadfence();
+          softmax_bar();
+          if (threadIdx.x == 0) s_merge = (atomicAdd(&A.unit_cnt[u], 1) == c1 - c0);
+          softmax_bar();
+          if (s_merge) {
+            // every segment of the unit is written: merge them into this
+            // thread's half row in slot order (the same sum whichever block
+            // merges) and reset the count for the next launch.  All loads of
+            // up to 4 segments are issued before they are used.
+            __threadfence();
+            if (valid) {
+              const int ns = c1 - c0 + 1;
+              const size_t s0 = (size_t)u + c0;
+              float M = -INFINITY, ls = 0.f;
+              float mk[4], lk[4];  // (max, sum) of up to 4 segments
+              for (int sb0 = 0; sb0 < ns; sb0 += 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  mk[k] = -INFINITY;
+                  lk[k] = 0.f;
+                  if (sb0 + k < ns) {
+                    const size_t row = (s0 + sb0 + k) * R + r;
+                    mk[k] = __ldcg(A.part_ml + row * 2);
+                    lk[k] = __ldcg(A.part_ml + row * 2 + 1);
+                  }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) M = fmaxf(M, mk[k]);
+              }
+#pragma unroll
+              for (int j = 0; j < 64; ++j) o[j] = 0.f;
+              for (int sb0 = 0; sb0 < ns; sb0 += 4) {
+                if (ns > 4) {  // several chunks: the first pass left the last one loaded
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    mk[k] = -INFINITY;
+                    lk[k] = 0.f;
+                    if (sb0 + k < ns) {
+                      const size_t row = (s0 + sb0 + k) * R + r;
+                      mk[k] = __ldcg(A.part_ml + row * 2);
+                      lk[k] = __ldcg(A.part_ml + row * 2 + 1);
+                    }
+                  }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int sg = sb0 + k;
+                  if (sg >= ns || mk[k] == -INFINITY) continue;
+                  const float wgt = exp2f(mk[k] - M);
+                  ls += lk[k] * wgt;
+                  const float4* src =
+                      reinterpret_cast<const float4*>(A.part_o) + ((s0 + sg) * 2 + h) * 16 * R + r;
+                  float4 t4[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) t4[j] = __ldcg(src + (size_t)j * R);
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    o[4 * j] += t4[j].x * wgt; o[4 * j + 1] += t4[j].y * wgt;
+                    o[4 * j + 2] += t4[j].z * wgt; o[4 * j + 3] += t4[j].w * wgt;
+                  }
+                }
+              }
+              const float inv = ls > 0.f ? 1.f / ls : 0.f;
+              bf16* dst = static_cast<bf16*>(A.o) +
+                          ((size_t)(b * W + p_row) * A.nq + kvh * G + r % G) * hd + h * 64;
+#pragma unroll
+              for (int j8 = 0; j8 < 8; ++j8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const __nv_bfloat162 t2 =
+                      __floats2bfloat162_rn(o[8 * j8 + 2 * k] * inv, o[8 * j8 + 2 * k + 1] * inv);
+                  w4[k] = *reinterpret_cast<const uint32_t*>(&t2);
+                }
+                reinterpret_cast<uint4*>(dst)[j8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            }
+            if (threadIdx.x == 0) A.unit_cnt[u] = 0;
           }
         }
         pair_bar();  // s_lsum is reused by the next segment
@@ -593,39 +714,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge the segment partials of every (window row, q head): one warp each,
-// lane = 4 head dims.  seg_table holds each unit's first segment slot and
-// segment count (written by block 0 of the attention kernel).
-__global__ void __launch_bounds__(256) attn_seg_merge_kernel(AttnArgs A) {
-  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (wid >= A.B * A.W * A.nq) return;
-  const int m = wid / A.nq, h = wid % A.nq;
-  const int b = m / A.W, p = m % A.W;
-  const int G = A.nq / A.nkv, kvh = h / G, g = h % G, R = G * A.W;
-  const int r = p * G + g;
-  const int u = b * A.nkv + kvh;
-  const int s0 = A.seg_table[u * 2 + 0], ns = A.seg_table[u * 2 + 1];
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, A.part_ml[((size_t)(s0 + s) * R + r) * 2]);
-  float lsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < ns; ++s) {
-    const size_t row = (size_t)(s0 + s) * R + r;
-    const float ms = A.part_ml[row * 2];
-    if (ms == -INFINITY) continue;
-    const float w = exp2f(ms - M);
-    lsum += A.part_ml[row * 2 + 1] * w;
-    const float4 o = __ldcg(reinterpret_cast<const float4*>(A.part_o + row * A.hd) + lane);
-    acc.x += o.x * w; acc.y += o.y * w; acc.z += o.z * w; acc.w += o.w * w;
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  __nv_bfloat162* dst =
-      reinterpret_cast<__nv_bfloat162*>(static_cast<bf16*>(A.o) + ((size_t)m * A.nq + h) * A.hd) +
-      2 * lane;
-  dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-}
-
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 attn_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -646,7 +734,7 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
                                 cudaStream_t st) {
   const int G = A.nq / A.nkv;
   if (A.hd != 128 || G * A.W > 128 || A.Wp > 64 || A.B > kMaxB || A.min_tiles < 1 ||
-      !A.seg_table || grid < 1 || (reinterpret_cast<uintptr_t>(A.q) & 15))
+      !A.unit_cnt || grid < 1 || (reinterpret_cast<uintptr_t>(A.q) & 15))
     return cudaErrorInvalidValue;
   AttnLayout Ly;
   Ly.R = G * A.W;
@@ -680,10 +768,6 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
   }
   const uint32_t smem = Ly.off_v + (uint32_t)Ly.VS * kKVBytes + 1024;
   attn_tc_kernel<<<std::min(grid, kMaxGrid), kThreads, smem, st>>>(mq, A, Ly, zero_page);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int warps = A.B * A.W * A.nq;
-  attn_seg_merge_kernel<<<(warps + 7) / 8, 256, 0, st>>>(A);
   return cudaGetLastError();
 }
 

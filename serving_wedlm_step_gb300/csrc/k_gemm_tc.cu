@@ -231,12 +231,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
 // that every partial is read once, coalesced.
 
 // sum of the splits at float4 index i of [M][N]
+// (loads four splits at a time; the additions stay in split order)
 __device__ __forceinline__ float4 splitk_sum4(const GemmProblem& P, size_t i) {
-  const float4* p4 = reinterpret_cast<const float4*>(P.partial);
+  const float4* p4 = reinterpret_cast<const float4*>(P.partial) + i;
   const size_t stride4 = (size_t)P.M * P.N / 4;
-  float4 a = __ldcg(p4 + i);
-  for (int sp = 1; sp < P.splits; ++sp) {
-    const float4 t = __ldcg(p4 + sp * stride4 + i);
+  float4 a = __ldcg(p4);
+  int sp = 1;
+  for (; sp + 3 < P.splits; sp += 4) {
+    float4 t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = __ldcg(p4 + (sp + k) * stride4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { a.x += t[k].x; a.y += t[k].y; a.z += t[k].z; a.w += t[k].w; }
+  }
+  for (; sp < P.splits; ++sp) {
+    const float4 t = __ldcg(p4 + sp * stride4);
     a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
   }
   return a;
@@ -253,6 +262,52 @@ __global__ void __launch_bounds__(256) splitk_resid_kernel(GemmProblem P) {
     const float2 x01 = __bfloat1622float2(xp[0]), x23 = __bfloat1622float2(xp[1]);
     xp[0] = __floats2bfloat162_rn(x01.x + a.x, x01.y + a.y);
     xp[1] = __floats2bfloat162_rn(x23.x + a.z, x23.y + a.w);
+  }
+}
+
+// RESID followed by the RMSNorm of the next GEMM's input: one block of
+// kNormThreads threads per activation row.  x[m] += acc[m] (bf16 rounding as in the plain
+// residual add), then xn[m] = x[m] * rsqrt(mean(x[m]^2) + eps) * norm_w from
+// the stored bf16 x, with the same per-thread 8-element vectors and the same
+// reduction order as rmsnorm_kernel, so the result is bit-identical to the
+// two separate kernels.
+__global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmProblem P) {
+  const int m = blockIdx.x;
+  const int n8 = P.N / 8;
+  bf16* x = static_cast<bf16*>(P.epi.x) + (size_t)m * P.N;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+    const float4 a0 = splitk_sum4(P, ((size_t)m * P.N) / 4 + 2 * i);
+    const float4 a1 = splitk_sum4(P, ((size_t)m * P.N) / 4 + 2 * i + 1);
+    const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    Vec16<bf16> v = ld16(x + 8 * i);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v.set(k, v.get(k) + a[k]);
+    st16(x + 8 * i, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float f = v.get(k);
+      ss = fmaf(f, f, ss);
+    }
+  }
+  __shared__ float red[32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)P.N + P.epi.eps);
+  const bf16* g = static_cast<const bf16*>(P.epi.norm_w);
+  bf16* xn = static_cast<bf16*>(P.epi.xn) + (size_t)m * P.N;
+  for (int i = threadIdx.x; i < n8; i += blockDim.x) {  // this thread's own stores
+    Vec16<bf16> v = ld16(x + 8 * i), gv = ld16(g + 8 * i), o;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o.set(k, v.get(k) * r * gv.get(k));
+    st16(xn + 8 * i, o);
   }
 }
 
@@ -490,12 +545,22 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + 1024;
   gemm_tc_kernel<<<grid, kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
-  if (launches_out) *launches_out = P.splits > 1 ? 2 : 1;
+  const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
+  if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
+  if (P.splits == 1 && norm) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
+                                static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
+                                static_cast<bf16*>(P.epi.xn), st);
+  }
   if (P.splits > 1) {
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int cap = plans.num_sms * 8;  // grid-stride beyond 8 blocks per SM
-    if (P.epi.mode == EPI_RESID) {
+    if (norm) {
+      splitk_resid_norm_kernel<<<P.M, kNormThreads, 0, st>>>(P);
+    } else if (P.epi.mode == EPI_RESID) {
       const size_t n4 = (size_t)P.M * P.N / 4;
       splitk_resid_kernel<<<(int)std::min<size_t>((n4 + 255) / 256, cap), 256, 0, st>>>(P);
     } else if (P.epi.mode == EPI_SWIGLU) {

@@ -116,7 +116,7 @@ cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, one block per row, fp32 math.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
                float eps, T* __restrict__ y) {
   constexpr int N = 16 / sizeof(T);
@@ -155,7 +155,7 @@ rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
 template <typename T>
 cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
                            T* y, cudaStream_t st) {
-  rmsnorm_kernel<T><<<M, 256, 0, st>>>(H, x, g, eps, y);
+  rmsnorm_kernel<T><<<M, kNormThreads, 0, st>>>(H, x, g, eps, y);
   return cudaGetLastError();
 }
 
