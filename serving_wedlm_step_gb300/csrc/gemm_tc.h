@@ -14,11 +14,13 @@ struct TcMapTable;  // TMA descriptors of every weight matrix
 // Everything the bf16 GEMMs need that is fixed at create time.
 struct TcPlanSet {
   int num_sms = 0;
+  int max_clusters[9] = {};  // clusters of S blocks (index S <= 8) resident at once
   size_t part_elems = 0;
   std::shared_ptr<TcMapTable> maps;
 };
 
-int tc_choose_splits(int tiles, int nkb, int M, int N, int num_sms, size_t part_elems);
+int tc_choose_splits(int tiles, int nkb, int M, int N, int ntile, int num_sms,
+                     size_t part_elems, double* time_out = nullptr);
 
 std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          const std::vector<LayerWeights>& layers,

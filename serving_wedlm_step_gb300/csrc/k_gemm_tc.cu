@@ -32,9 +32,9 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kBK = 64;                           // K elements per stage (128 bytes)
 constexpr uint32_t kXBlockBytes = 128 * kBK * 2;  // one activation row block
-constexpr uint32_t kWBoxBytes = 64 * kBK * 2;     // one 64-row weight box
 constexpr int kThreads = 192;                     // producer, MMA, 4 epilogue warps
 constexpr int kMaxDynSmem = 221 * 1024;
+constexpr int kMaxCluster = 8;                    // portable cluster sizes
 
 __device__ __forceinline__ void epi_bar() {       // the 4 epilogue warps only
   asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -50,11 +50,31 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 }
 }  // namespace
 
+// all threads of all blocks of the cluster (release / acquire)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of the same shared-memory location in block `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+
 struct TcLaunch {
   int stages, ntile, nrb, nbuf, tiles;
   uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
 };
 
+// kCluster: split-K inside a thread-block cluster of P.splits blocks (one
+// unit per block, cluster rank = split); the splits are added through
+// distributed shared memory instead of global partials.
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mX,
@@ -103,7 +123,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       const uint64_t pol = l2_evict_first_policy();
-      const int nbox = ntile / 64, hb = nbox / 2, half = ntile / 2;
+      const int half = ntile / 2;
       int it = 0;
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
@@ -125,17 +145,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           const int kx = kb * kBK;
           for (int r = 0; r < L.nrb; ++r)
             tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
-          for (int j = 0; j < nbox; ++j) {
-            const CUtensorMap* mp;
-            int row;
-            if (P.swiglu) {  // first half of the boxes: gate rows, second half: up rows
-              mp = j < hb ? &mW0 : &mW1;
-              row = tile * half + 64 * (j < hb ? j : j - hb);
-            } else {
-              mp = seg;
-              row = row0 + 64 * j;
-            }
-            tma_load_2d_hint(st + L.a_bytes + j * kWBoxBytes, mp, &bar_full[s], kx, row, pol);
+          // the weight tile in one box (SwiGLU: gate rows, then up rows);
+          // rows of 128 bytes one after another, as the MMA descriptors expect
+          if (P.swiglu) {
+            tma_load_2d_hint(st + L.a_bytes, &mW0, &bar_full[s], kx, tile * half, pol);
+            tma_load_2d_hint(st + L.a_bytes + half * 128, &mW1, &bar_full[s], kx, tile * half, pol);
+          } else {
+            tma_load_2d_hint(st + L.a_bytes, seg, &bar_full[s], kx, row0, pol);
           }
         }
       }
@@ -192,8 +208,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols +
                                (uint32_t)(r * ntile);
         if (P.splits == 1) {
-          AccRow a{1, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
+          AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
+        } else if (kCluster) {
+          // the accumulator stays in TMEM for the exchange below
         } else {
           float* dst = P.partial + (size_t)split * P.M * P.N + (size_t)m * P.N + tile * ntile;
           for (int c = 0; c < ntile; c += 32) {
@@ -212,6 +230,45 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);  // accumulator free for the MMA warp
+    }
+  }
+  if constexpr (kCluster) {
+    // Row group g (TMEM lanes 32g..32g+31) of the tile belongs to cluster
+    // rank g % S.  Every block sends its rows of each group to the group's
+    // owner, column by column ([column][32 rows]: each warp store is 128
+    // contiguous bytes); the owner adds the S contributions in rank order
+    // and runs the epilogue on its rows, 4 warps splitting the epilogue items.
+    const int S = P.splits, rank = (int)(blockIdx.x % S), tile = (int)(blockIdx.x / S);
+    const int grp = 32 * ntile;             // floats of one group contribution
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();  // every block's main loop is done: shared memory is free
+    tc_fence_after();
+    if (warp >= 2) {
+      const int g = warp & 3, owner = g % S, lg = g / S;
+      const uint32_t local = smem_u32(base) + (uint32_t)(((lg * S + rank) * grp + lane) * 4);
+      const uint32_t remote = cluster_addr(local, (uint32_t)owner);
+      const uint32_t taddr = tmem + ((uint32_t)(32 * g) << 16);
+      for (int c = 0; c < ntile; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_cluster_f32(remote + (uint32_t)((c + j) * 128), v[j]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();  // every contribution has landed
+    tc_fence_after();
+    if (warp >= 2) {
+      const int items = tc_epi_items(P, ntile);
+      for (int lg = 0; rank + lg * S < 4; ++lg) {
+        const int m = 32 * (rank + lg * S) + lane;
+        const float* part = reinterpret_cast<const float*>(base) + (size_t)(lg * S) * grp + lane;
+        AccRow a{ACC_SMEM, 0, part, (size_t)grp, S, tile * ntile, P.N, m < P.M};
+        for (int it = warp - 2; it < items; it += 4)
+          tc_epilogue_rows(P, a, m, tile, ntile, it, it + 1);
+      }
     }
   }
   tc_fence_before();
@@ -394,7 +451,7 @@ splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
   const int tile = blockIdx.x / items, item = blockIdx.x % items;
   const int m = blockIdx.y * 128 + threadIdx.x;
   const float* src = P.partial + (size_t)min(m, P.M - 1) * P.N + tile * ntile;
-  AccRow a{0, 0, src, (size_t)P.M * P.N, P.splits, tile * ntile, P.N, m < P.M};
+  AccRow a{ACC_PARTIAL, 0, src, (size_t)P.M * P.N, P.splits, tile * ntile, P.N, m < P.M};
   tc_epilogue_rows(P, a, m, tile, ntile, item, item + 1);
 }
 
@@ -434,9 +491,14 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint3
 
 }  // namespace
 
+// weight descriptors for boxes of 64, 128 and 256 rows (x 64 K elements):
+// a GEMM loads its whole weight tile (or each SwiGLU half) in one box
 struct TcMapTable {
-  std::unordered_map<const void*, CUtensorMap> weight;
+  std::unordered_map<const void*, CUtensorMap> weight[3];
 };
+namespace {
+int box_slot(int rows) { return rows == 64 ? 0 : rows == 128 ? 1 : rows == 256 ? 2 : -1; }
+}
 
 std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          const std::vector<LayerWeights>& layers,
@@ -449,9 +511,13 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
   p->part_elems = part_elems;
   p->maps = std::make_shared<TcMapTable>();
   auto add = [&](const void* w, uint64_t rows, uint64_t K) {
-    CUtensorMap m;
-    if (!encode_2d(&m, w, K, rows, 64)) return false;
-    p->maps->weight[w] = m;
+    for (int b = 0; b < 3; ++b) {
+      const uint32_t box = 64u << b;
+      if (box > rows) continue;
+      CUtensorMap m;
+      if (!encode_2d(&m, w, K, rows, box)) return false;
+      p->maps->weight[b][w] = m;
+    }
     return true;
   };
   const uint64_t H = g.hidden, hd = g.head_dim;
@@ -471,33 +537,69 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
     return nullptr;
   }
   // dynamic shared memory: up to 220 KB of stages + 1 KB alignment slack
-  const cudaError_t e = cudaFuncSetAttribute(
-      gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxDynSmem);
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (msg) *msg = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return nullptr;
   }
+  // clusters of S blocks that fit on the GPU at once (0: none)
+  for (int S = 2; S <= kMaxCluster; ++S) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kMaxDynSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    p->max_clusters[S] = n;
+  }
   return p;
 }
 
 // split-K factor for the persistent kernel: units = tiles * s are dealt
-// round-robin to num_sms blocks.  Cost in k-block times: the busiest
-// block's k-blocks (+1 per unit for the handoff), plus for s > 1 a second
-// launch and the fp32 partial round trip (s * M * N * 8 bytes through L2,
-// about 12 k-block times per 64 MB); >= 4 k-blocks per unit
-int tc_choose_splits(int tiles, int nkb, int M, int N, int num_sms, size_t part_elems) {
+// round-robin to num_sms blocks.  Modelled time: the weight stream is bound
+// by the busiest block (about 65 GB/s for one SM streaming one-box weight
+// tiles with its activation blocks) or by the whole GPU (about 6.5 TB/s),
+// whichever is slower; split-K adds a second launch (about 3 us) and the
+// fp32 partial round trip (s * M * N * 8 bytes at about 2 TB/s effective).
+// At least 4 k-blocks per unit.
+int tc_choose_splits(int tiles, int nkb, int M, int N, int ntile, int num_sms,
+                     size_t part_elems, double* time_out) {
+  const double w_kb = (double)ntile * kBK * 2, x_kb = (double)((M + 127) / 128) * kXBlockBytes;
+  const double t_all = (double)tiles * nkb * w_kb / 6.5e12;
   int best = 1;
-  double best_cost = 1e30;
+  double best_t = 1e30;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && (nkb / s < 4 || (size_t)s * M * N > part_elems)) break;
     const int rounds = (tiles * s + num_sms - 1) / num_sms;
     const int kper = (nkb + s - 1) / s;
-    const double partial_mb = (double)s * M * N * 8.0 / 1e6;
-    const double cost = (double)rounds * (kper + 1.0) + (s > 1 ? 3.0 + 12.0 * partial_mb / 64.0 : 0.0);
-    if (cost < best_cost - 1e-9) { best_cost = cost; best = s; }
+    const double t_sm = (double)rounds * kper * (w_kb + x_kb) / 65e9;
+    double t = std::max(t_sm, t_all);
+    if (s > 1) t += 3e-6 + (double)s * M * N * 8.0 / 2e12;
+    if (t < best_t * (1.0 - 1e-9)) { best_t = t; best = s; }
   }
+  if (time_out) *time_out = best_t;
   return best;
+}
+
+// shared memory one block of a cluster needs for the split-K exchange: the
+// rank-0 block owns ceil(4 / S) row groups, each S contributions of 32 rows
+size_t tc_cluster_xbytes(int S, int ntile) {
+  return (size_t)((4 + S - 1) / S) * S * 32 * ntile * 4;
 }
 
 // output features per tile: 256 when one 128-row block of activations
@@ -515,16 +617,50 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
                            int* tiles_out, int* launches_out) {
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
+  const int nkb = P.K / kBK;
+  const int wmax = tc_tile_width(P);
+  auto tiles_for = [&](int ntile) {
+    return P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
+  };
+  // the plan: the persistent kernel (split-K through global partials when
+  // splits > 1) or split-K inside clusters of S blocks.  Clusters serve the
+  // per-head QKV epilogue of one 128-row block of activations: there they
+  // beat the global partials (measured 29 vs 34 us for the Qwen3-8B shape);
+  // the residual epilogues keep the persistent path, whose split-K
+  // epilogue also fuses the next RMSNorm.  Modelled like tc_choose_splits
+  // (one wave of clusters, about 2 us for the exchange).
+  bool cluster = false;
+  int ntile = wmax;
+  double best_t = 0.0;
+  int splits = tc_choose_splits(tiles_for(wmax), nkb, P.M, P.N, wmax, plans.num_sms,
+                                plans.part_elems, &best_t);
+  if (P.M <= 128 && P.epi.mode == EPI_QKV) {
+    for (int nt = wmax; nt >= 128; nt /= 2) {
+      if (nt != wmax && (P.swiglu || P.N % nt)) break;
+      const int tiles = tiles_for(nt);
+      const double w_kb = (double)nt * kBK * 2, t_all = (double)tiles * nkb * w_kb / 6.5e12;
+      for (int S = 2; S <= kMaxCluster; ++S) {
+        if (nkb / S < 4 || tiles > plans.max_clusters[S] ||
+            tc_cluster_xbytes(S, nt) > (size_t)kMaxDynSmem - 1024)
+          continue;
+        const int kper = (nkb + S - 1) / S;
+        const double t = std::max(kper * (w_kb + kXBlockBytes) / 65e9, t_all) + 2e-6;
+        if (t < best_t * (1.0 - 1e-9)) { best_t = t; cluster = true; ntile = nt; splits = S; }
+      }
+    }
+  }
+  const int bslot = box_slot(P.swiglu ? ntile / 2 : ntile);
+  if (bslot < 0) return cudaErrorInvalidValue;
   auto find = [&](const void* w) -> const CUtensorMap* {
-    auto it = plans.maps->weight.find(w);
-    return it == plans.maps->weight.end() ? nullptr : &it->second;
+    auto it = plans.maps->weight[bslot].find(w);
+    return it == plans.maps->weight[bslot].end() ? nullptr : &it->second;
   };
   const CUtensorMap* a0 = find(P.A0);
   const CUtensorMap* a1 = find(P.A1);
   const CUtensorMap* a2 = find(P.A2);
   if (!a0 || !a1 || !a2) return cudaErrorInvalidValue;
   TcLaunch L;
-  L.ntile = tc_tile_width(P);
+  L.ntile = ntile;
   L.nrb = (P.M + 127) / 128;
   L.buf_cols = (uint32_t)(L.nrb * L.ntile);
   L.nbuf = L.buf_cols * 2 <= 512 ? 2 : 1;
@@ -538,14 +674,38 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   L.tmem_cols = cols;
   CUtensorMap mx;
   if (!encode_2d(&mx, P.X, P.K, P.M, 128)) return cudaErrorInvalidValue;
-  L.tiles = P.swiglu ? (P.N / 2) / (L.ntile / 2) : (P.N + L.ntile - 1) / L.ntile;
+  L.tiles = tiles_for(ntile);
   if (tiles_out) *tiles_out = L.tiles;
-  P.splits = tc_choose_splits(L.tiles, P.K / kBK, P.M, P.N, plans.num_sms, plans.part_elems);
+  P.splits = splits;
   const int units = L.tiles * P.splits;
+  const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
+  if (cluster) {
+    size_t smem = (size_t)L.stages * L.stage_bytes;
+    smem = std::max(smem, tc_cluster_xbytes(P.splits, ntile)) + 1024;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = P.splits;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, *a0, *a1, *a2, mx, P, L);
+    if (launches_out) *launches_out = norm ? 2 : 1;
+    if (e != cudaSuccess) return e;
+    if (norm)
+      return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
+                                  static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
+                                  static_cast<bf16*>(P.epi.xn), st);
+    return cudaGetLastError();
+  }
   const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + 1024;
-  gemm_tc_kernel<<<grid, kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
-  const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
+  gemm_tc_kernel<false><<<grid, kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
   if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
   if (P.splits == 1 && norm) {
     const cudaError_t e = cudaGetLastError();

@@ -130,6 +130,11 @@ WORKLOADS = {
     "full_stack": Workload("full_stack", QWEN3_8B, batch=8, window=16,
                            prefix=4096, masked=16, all_masked_start=True,
                            steps=256, seed=0, extra_pages=256),
+    # the full_stack shapes with 2 layers: small enough (about 3.5 GB on the
+    # device) for profiler captures of the same kernels
+    "two_layer": Workload("two_layer", qwen3_layers(2), batch=8, window=16,
+                          prefix=4096, masked=16, all_masked_start=True,
+                          steps=256, seed=0, extra_pages=256),
     # low-entropy long context: prefix 32768, W=32, batch 8, planted
     # peaked next-token bias on a seeded counting sequence
     "low_entropy": Workload("low_entropy", QWEN3_8B, batch=8, window=32,
