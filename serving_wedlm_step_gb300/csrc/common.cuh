@@ -68,6 +68,18 @@ __device__ __forceinline__ int tile_off(int t, int d, int hd) {
   return (((t >> 3) * (hd >> 3) + (d >> 3)) << 6) + ((t & 7) << 3) + (d & 7);
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may
+// start while the previous kernel on the stream is still running: before
+// reading anything that kernel wrote, and before writing anything, it calls
+// pdl_wait (which returns once the previous kernel has completed and its
+// memory is visible), then pdl_trigger lets the next kernel start early in
+// turn.  Work on data no kernel of the step writes (weights, cached KV pages,
+// page tables) may go before pdl_wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_err(int* err, int bits) {
   if (err) atomicOr(err, bits);
 }

@@ -1,6 +1,8 @@
 // Internal launch interfaces of libwedlm (host side).
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -10,6 +12,24 @@
 #include "common.cuh"
 
 namespace wedlm {
+
+// Launch with programmatic stream serialization (see pdl_wait): the kernel
+// must call pdl_wait before touching the previous kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // threads of one RMSNorm block (one block per row); the fused residual +
 // norm epilogue uses the same count so that both reduce in the same order

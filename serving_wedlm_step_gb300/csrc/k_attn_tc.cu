@@ -331,22 +331,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       const size_t blockn = (size_t)kPageBlock * hd;
       constexpr int kPg = kPagesPerTile;
       if (!kv) tma_prefetch_desc(&mq);
+      // a new segment's Q goes into buffer seg & 1 once the S MMAs of the
+      // segment two back are done with it
+      auto issue_q = [&](int sg, int b, int kvh) -> bool {
+        const int qb = sg & 1;
+        if (!wait(&q_empty[qb], ((uint32_t)(sg >> 1) & 1u) ^ 1u)) return false;
+        uint8_t* qdst = base + qb * Ly.q_bytes;
+        mbar_arrive_expect_tx(&q_full[qb], (uint32_t)(16 * R * 16));
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c)
+          tma_load_3d(qdst + c * Ly.Rpad * 16, &mq, &q_full[qb], 8 * c, kvh * G, b * W);
+        s_issued[2] = sg + 1;
+        return true;
+      };
+      // Cached K/V pages do not depend on the previous kernel (the QKV
+      // projection): the first ring of prefix tiles is copied before
+      // waiting for it; Q and the window tile (both its outputs) after.
+      bool waited = false;
+      int nq_def = 0, qdef_seg[kMaxStages], qdef_b[kMaxStages], qdef_h[kMaxStages];
+      auto wait_prev = [&]() -> bool {
+        pdl_wait();
+        if (!kv) pdl_trigger();
+        waited = true;
+        for (int j = 0; j < nq_def; ++j)
+          if (!issue_q(qdef_seg[j], qdef_b[j], qdef_h[j])) return false;
+        nq_def = 0;
+        return true;
+      };
       int seg = -1;
       Cur cur = first;
       for (int i = 0; i < ntiles; ++i, advance(cur)) {
         const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
+        if (!waited && (i == NS || t == T - 1) && !wait_prev()) break;
         if (!kv && (i == 0 || t == 0)) {
-          // a new segment: its Q into buffer seg & 1, once the S MMAs of the
-          // segment two back are done with it
           ++seg;
-          const int qb = seg & 1;
-          if (!wait(&q_empty[qb], ((uint32_t)(seg >> 1) & 1u) ^ 1u)) break;
-          uint8_t* qdst = base + qb * Ly.q_bytes;
-          mbar_arrive_expect_tx(&q_full[qb], (uint32_t)(16 * R * 16));
-#pragma unroll 1
-          for (int c = 0; c < 16; ++c)
-            tma_load_3d(qdst + c * Ly.Rpad * 16, &mq, &q_full[qb], 8 * c, kvh * G, b * W);
-          s_issued[2] = seg + 1;
+          if (waited) {
+            if (!issue_q(seg, b, kvh)) break;
+          } else {
+            qdef_seg[nq_def] = seg;
+            qdef_b[nq_def] = b;
+            qdef_h[nq_def] = kvh;
+            ++nq_def;
+          }
         }
         int pid[kPg];
 #pragma unroll
@@ -389,6 +415,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         }
         s_issued[kv] = i + 1;
       }
+      if (!waited) wait_prev();
     }
   } else if (warp == 9) {
     if (lane == 0) {
@@ -460,6 +487,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     }
   } else {
     // ---------------- softmax warps ----------------
+    pdl_wait();  // they write the outputs (and read nothing else of the previous kernel)
     const int q = warp & 3, h = warp >> 2;       // lane quadrant, key / dim half
     const int r = 32 * q + lane;                  // query row
     const bool valid = r < R;
@@ -767,8 +795,8 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
     attr = true;
   }
   const uint32_t smem = Ly.off_v + (uint32_t)Ly.VS * kKVBytes + 1024;
-  attn_tc_kernel<<<std::min(grid, kMaxGrid), kThreads, smem, st>>>(mq, A, Ly, zero_page);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel, dim3(std::min(grid, kMaxGrid)), dim3(kThreads), smem, st, mq,
+                    A, Ly, zero_page);
 }
 
 }  // namespace wedlm

@@ -126,6 +126,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       const int half = ntile / 2;
       int it = 0;
       bool alive = true;
+      // weights do not depend on the previous kernel: the first ring of
+      // weight boxes goes out before waiting for it, their activation boxes
+      // once it is done
+      bool waited = false;
+      int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
+      auto issue_x = [&](int s, int kx) {
+        uint8_t* st = base + (size_t)s * L.stage_bytes;
+        for (int r = 0; r < L.nrb; ++r)
+          tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
+      };
+      auto wait_prev = [&]() {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+        for (int j = 0; j < npend; ++j) issue_x(pend_s[j], pend_kx[j]);
+        npend = 0;
+      };
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
         const int tile = u / P.splits, split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
@@ -143,8 +160,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           uint8_t* st = base + (size_t)s * L.stage_bytes;
           mbar_arrive_expect_tx(&bar_full[s], L.stage_bytes);
           const int kx = kb * kBK;
-          for (int r = 0; r < L.nrb; ++r)
-            tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
           // the weight tile in one box (SwiGLU: gate rows, then up rows);
           // rows of 128 bytes one after another, as the MMA descriptors expect
           if (P.swiglu) {
@@ -153,8 +168,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           } else {
             tma_load_2d_hint(st + L.a_bytes, seg, &bar_full[s], kx, row0, pol);
           }
+          if (waited) {
+            issue_x(s, kx);
+          } else {
+            pend_s[npend] = s;
+            pend_kx[npend] = kx;
+            if (++npend == L.stages) wait_prev();
+          }
         }
       }
+      if (!waited) wait_prev();
       s_issued = it;
     }
   } else if (warp == 1) {
@@ -193,6 +216,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     }
   } else {
     // ---------------- epilogue warps: thread = activation row ----------------
+    pdl_wait();  // outputs and partials may still be read by the previous kernel
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int ul = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
@@ -310,6 +334,8 @@ __device__ __forceinline__ float4 splitk_sum4(const GemmProblem& P, size_t i) {
 
 // RESID: x[m][n] += acc[m][n]
 __global__ void __launch_bounds__(256) splitk_resid_kernel(GemmProblem P) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const size_t n4 = (size_t)P.M * P.N / 4;
   bf16* x = static_cast<bf16*>(P.epi.x);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
@@ -329,6 +355,8 @@ __global__ void __launch_bounds__(256) splitk_resid_kernel(GemmProblem P) {
 // reduction order as rmsnorm_kernel, so the result is bit-identical to the
 // two separate kernels.
 __global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmProblem P) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int m = blockIdx.x;
   const int n8 = P.N / 8;
   bf16* x = static_cast<bf16*>(P.epi.x) + (size_t)m * P.N;
@@ -372,6 +400,8 @@ __global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmPro
 // [t*half, (t+1)*half) in columns [0, half) and the same up features in
 // [half, ntile)
 __global__ void __launch_bounds__(256) splitk_swiglu_kernel(GemmProblem P, int ntile) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int half = ntile / 2, F = P.N / 2;
   const size_t n4 = (size_t)P.M * F / 4;
   bf16* act = static_cast<bf16*>(P.epi.act);
@@ -397,6 +427,8 @@ __global__ void __launch_bounds__(256) splitk_swiglu_kernel(GemmProblem P, int n
 // (d, d + 64), which sit in lanes l and l ^ 16; q goes to q_out, k and v
 // to the layer's window scratch in the 8x8-tile layout.
 __global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const GemmEpi& e = P.epi;
   const int lane = threadIdx.x & 31;
   const int heads = P.N / 128;
@@ -448,6 +480,8 @@ __global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
 // any other epilogue: thread = (activation row, epilogue item)
 __global__ void __launch_bounds__(128)
 splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int tile = blockIdx.x / items, item = blockIdx.x % items;
   const int m = blockIdx.y * 128 + threadIdx.x;
   const float* src = P.partial + (size_t)min(m, P.M - 1) * P.N + tile * ntile;
@@ -687,13 +721,15 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = P.splits;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, *a0, *a1, *a2, mx, P, L);
     if (launches_out) *launches_out = norm ? 2 : 1;
     if (e != cudaSuccess) return e;
@@ -705,34 +741,34 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   }
   const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + 1024;
-  gemm_tc_kernel<false><<<grid, kThreads, smem, st>>>(*a0, *a1, *a2, mx, P, L);
+  cudaError_t le = launch_pdl(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, st, *a0, *a1,
+                              *a2, mx, P, L);
   if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
+  if (le != cudaSuccess) return le;
   if (P.splits == 1 && norm) {
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
                                 static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
                                 static_cast<bf16*>(P.epi.xn), st);
   }
   if (P.splits > 1) {
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const int cap = plans.num_sms * 8;  // grid-stride beyond 8 blocks per SM
     if (norm) {
-      splitk_resid_norm_kernel<<<P.M, kNormThreads, 0, st>>>(P);
+      return launch_pdl(splitk_resid_norm_kernel, dim3(P.M), dim3(kNormThreads), 0, st, P);
     } else if (P.epi.mode == EPI_RESID) {
       const size_t n4 = (size_t)P.M * P.N / 4;
-      splitk_resid_kernel<<<(int)std::min<size_t>((n4 + 255) / 256, cap), 256, 0, st>>>(P);
+      return launch_pdl(splitk_resid_kernel, dim3((int)std::min<size_t>((n4 + 255) / 256, cap)),
+                        dim3(256), 0, st, P);
     } else if (P.epi.mode == EPI_SWIGLU) {
       const size_t n4 = (size_t)P.M * (P.N / 2) / 4;
-      splitk_swiglu_kernel<<<(int)std::min<size_t>((n4 + 255) / 256, cap), 256, 0, st>>>(
-          P, L.ntile);
+      return launch_pdl(splitk_swiglu_kernel, dim3((int)std::min<size_t>((n4 + 255) / 256, cap)),
+                        dim3(256), 0, st, P, L.ntile);
     } else if (P.epi.mode == EPI_QKV && P.epi.hd == 128) {
       const int warps = P.M * (P.N / 128);
-      splitk_qkv_kernel<<<(warps + 7) / 8, 256, 0, st>>>(P);
+      return launch_pdl(splitk_qkv_kernel, dim3((warps + 7) / 8), dim3(256), 0, st, P);
     } else {
       const int items = tc_epi_items(P, L.ntile);
-      splitk_epilogue_kernel<<<dim3(L.tiles * items, L.nrb), 128, 0, st>>>(P, L.ntile, items);
+      return launch_pdl(splitk_epilogue_kernel, dim3(L.tiles * items, L.nrb), dim3(128), 0, st, P,
+                        L.ntile, items);
     }
   }
   return cudaGetLastError();

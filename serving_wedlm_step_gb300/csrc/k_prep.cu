@@ -33,6 +33,8 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
                      int32_t* perm_ws, int32_t* inv_ws, int32_t* pos_phys,
                      int32_t* seq_snap, int32_t* plant_phys, T* x,
                      float* cosb, float* sinb, int* err) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int p = blockIdx.x, b = blockIdx.y;
   __shared__ int s_slot;
   if (threadIdx.x == 0) {
@@ -90,11 +92,9 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  int32_t* pos_phys, int32_t* seq_snap,
                                  int32_t* plant_phys, T* x, float* cosb,
                                  float* sinb, int* err, cudaStream_t st) {
-  reorder_embed_kernel<T><<<dim3(W, B), 128, 0, st>>>(
-      W, H, hd, vocab, page_cap, tokens, pos, obs, seq_len, plant, embed,
-      inv_freq, perm_ws, inv_ws, pos_phys, seq_snap, plant_phys, x, cosb,
-      sinb, err);
-  return cudaGetLastError();
+  return launch_pdl(reorder_embed_kernel<T>, dim3(W, B), dim3(128), 0, st, W, H, hd, vocab,
+                    page_cap, tokens, pos, obs, seq_len, plant, embed, inv_freq, perm_ws,
+                    inv_ws, pos_phys, seq_snap, plant_phys, x, cosb, sinb, err);
 }
 
 __global__ void rope_table_kernel(int hd, const int32_t* __restrict__ pos_phys,
@@ -119,6 +119,8 @@ template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
                float eps, T* __restrict__ y) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   constexpr int N = 16 / sizeof(T);
   const int m = blockIdx.x;
   const T* xr = x + (size_t)m * H;
@@ -155,8 +157,7 @@ rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
 template <typename T>
 cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
                            T* y, cudaStream_t st) {
-  rmsnorm_kernel<T><<<M, kNormThreads, 0, st>>>(H, x, g, eps, y);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel<T>, dim3(M), dim3(kNormThreads), 0, st, H, x, g, eps, y);
 }
 
 #define INST(T)                                                               \

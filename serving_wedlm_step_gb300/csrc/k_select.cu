@@ -35,6 +35,8 @@ __global__ void lmhead_merge_kernel(int M, int tiles,
                                     const SoftmaxPart* __restrict__ part,
                                     wedlm_slot_rec* __restrict__ rows,
                                     int* err) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= M) return;
@@ -70,8 +72,8 @@ cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 cudaStream_t st) {
   const int threads = 128;
   const int blocks = (M * 32 + threads - 1) / threads;
-  lmhead_merge_kernel<<<blocks, threads, 0, st>>>(M, tiles, part, rows, err);
-  return cudaGetLastError();
+  return launch_pdl(lmhead_merge_kernel, dim3(blocks), dim3(threads), 0, st, M, tiles, part, rows,
+                    err);
 }
 
 // ---------------------------------------------------------------------------
@@ -79,6 +81,8 @@ cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
 // sequence, thread j = slot j
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kMaxWindow) select_kernel(SelArgs S) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   const int b = blockIdx.x, j = threadIdx.x, W = S.W;
   __shared__ int s_obs[kMaxWindow], s_pos[kMaxWindow], s_tok[kMaxWindow];
   __shared__ int s_sel[kMaxWindow], s_fill_tok[kMaxWindow];
@@ -157,8 +161,7 @@ __global__ void __launch_bounds__(kMaxWindow) select_kernel(SelArgs S) {
 }
 
 cudaError_t launch_select(const SelArgs& S, cudaStream_t st) {
-  select_kernel<<<S.B, kMaxWindow, 0, st>>>(S);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(S.B), dim3(kMaxWindow), 0, st, S);
 }
 
 // ---------------------------------------------------------------------------
@@ -167,6 +170,8 @@ cudaError_t launch_select(const SelArgs& S, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(128) commit_kernel(CommitArgs C) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
   constexpr int VN = 16 / sizeof(T);
   const int b = blockIdx.x;
   const int y = blockIdx.y;
@@ -192,8 +197,7 @@ __global__ void __launch_bounds__(128) commit_kernel(CommitArgs C) {
 
 template <typename T>
 cudaError_t launch_commit(const CommitArgs& C, cudaStream_t st) {
-  commit_kernel<T><<<dim3(C.B, C.n_layers * 2 * C.nkv), 128, 0, st>>>(C);
-  return cudaGetLastError();
+  return launch_pdl(commit_kernel<T>, dim3(C.B, C.n_layers * 2 * C.nkv), dim3(128), 0, st, C);
 }
 
 template cudaError_t launch_commit<float>(const CommitArgs&, cudaStream_t);
