@@ -71,6 +71,13 @@ __device__ __forceinline__ void st_bf16x32(bf16* dst, const float (&v)[32]) {
   }
 }
 
+// SiLU x / (1 + e^-x) without branches: __expf and __fdividef (a few ulp,
+// far below the bf16 rounding of the result; for x below about -87 the
+// denominator overflows and the result is 0, the limit)
+__device__ __forceinline__ float silu_fast(float x) {
+  return __fdividef(x, 1.0f + __expf(-x));
+}
+
 // Epilogue items of a tile: independent pieces of one row's work.
 // RESID: 32-column chunks; SWIGLU: 32-feature chunks (gate + up columns);
 // QKV: heads; LMHEAD: the whole tile (one item).
@@ -110,7 +117,7 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
       acc_chunk(a, c, g);
       acc_chunk(a, half + c, u);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.0f + expf(-g[j])) * u[j];
+      for (int j = 0; j < 32; ++j) g[j] = silu_fast(g[j]) * u[j];
       if (a.valid) st_bf16x32(out + c, g);
     }
   } else if (e.mode == EPI_QKV) {

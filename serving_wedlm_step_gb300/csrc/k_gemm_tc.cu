@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(256) splitk_swiglu_kernel(GemmProblem P, int n
     const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
     float o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = gv[k] / (1.0f + expf(-gv[k])) * uv[k];
+    for (int k = 0; k < 4; ++k) o[k] = silu_fast(gv[k]) * uv[k];
     __nv_bfloat162* ap = reinterpret_cast<__nv_bfloat162*>(act + e);
     ap[0] = __floats2bfloat162_rn(o[0], o[1]);
     ap[1] = __floats2bfloat162_rn(o[2], o[3]);
@@ -525,13 +525,19 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint3
 
 }  // namespace
 
-// weight descriptors for boxes of 64, 128 and 256 rows (x 64 K elements):
-// a GEMM loads its whole weight tile (or each SwiGLU half) in one box
+// weight descriptors for boxes of 64, 96, 128 and 256 rows (x 64 K
+// elements): a GEMM loads its whole weight tile (or each SwiGLU half) in one
+// box
+constexpr int kBoxRows[4] = {64, 96, 128, 256};
 struct TcMapTable {
-  std::unordered_map<const void*, CUtensorMap> weight[3];
+  std::unordered_map<const void*, CUtensorMap> weight[4];
 };
 namespace {
-int box_slot(int rows) { return rows == 64 ? 0 : rows == 128 ? 1 : rows == 256 ? 2 : -1; }
+int box_slot(int rows) {
+  for (int b = 0; b < 4; ++b)
+    if (kBoxRows[b] == rows) return b;
+  return -1;
+}
 }
 
 std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
@@ -545,8 +551,8 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
   p->part_elems = part_elems;
   p->maps = std::make_shared<TcMapTable>();
   auto add = [&](const void* w, uint64_t rows, uint64_t K) {
-    for (int b = 0; b < 3; ++b) {
-      const uint32_t box = 64u << b;
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t box = (uint32_t)kBoxRows[b];
       if (box > rows) continue;
       CUtensorMap m;
       if (!encode_2d(&m, w, K, rows, box)) return false;
@@ -668,6 +674,15 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   double best_t = 0.0;
   int splits = tc_choose_splits(tiles_for(wmax), nkb, P.M, P.N, wmax, plans.num_sms,
                                 plans.part_elems, &best_t);
+  if (P.swiglu) {  // narrower tiles spread the gate/up features over more SMs
+    for (int nt : {192, 128}) {
+      if (nt >= wmax || (P.N / 2) % (nt / 2)) continue;
+      double t = 0.0;
+      const int s = tc_choose_splits(tiles_for(nt), nkb, P.M, P.N, nt, plans.num_sms,
+                                     plans.part_elems, &t);
+      if (t < best_t * (1.0 - 1e-9)) { best_t = t; ntile = nt; splits = s; }
+    }
+  }
   if (P.M <= 128 && P.epi.mode == EPI_QKV) {
     for (int nt = wmax; nt >= 128; nt /= 2) {
       if (nt != wmax && (P.swiglu || P.N % nt)) break;
