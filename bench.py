@@ -53,6 +53,22 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def reduce_over_ranks(ms, committed, world, device):
+    """Whole-job numbers of independent replicas: the slowest rank's time and
+    the tokens every rank committed (no collective touches the data path;
+    this is the only exchange, after the timed region)."""
+    if world <= 1:
+        return ms, committed
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, committed], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), int(sm[1])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -245,14 +261,7 @@ def run_ours(args):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     committed = int(seq_len.sum()) - len0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, committed], dtype=torch.float64, device=device)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = t.clone()
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        ms, committed = float(mx[0]), int(sm[1])
+    ms, committed = reduce_over_ranks(ms, committed, world, device)
     if ctx.status() != 0:
         raise RuntimeError("device error word set during the timed steps")
     value = committed / (ms / 1e3)
