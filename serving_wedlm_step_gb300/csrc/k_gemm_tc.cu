@@ -642,11 +642,12 @@ size_t tc_cluster_xbytes(int S, int ntile) {
   return (size_t)((4 + S - 1) / S) * S * 32 * ntile * 4;
 }
 
-// output features per tile: 256 when one 128-row block of activations
-// leaves room for two 256-column TMEM accumulators, else 128; every
-// segment boundary (q|k|v) must fall on a tile boundary
+// widest tile of output features: 256 while the 128-row activation blocks
+// fit one 256-column TMEM accumulator each (up to 256 rows; one accumulator
+// buffer instead of two above 128 rows), else 128; every segment boundary
+// (q|k|v) must fall on a tile boundary
 int tc_tile_width(const GemmProblem& P) {
-  if (P.M > 128) return 128;
+  if (P.M > 256) return 128;
   if (P.swiglu) return (P.N / 2) % 128 == 0 ? 256 : 128;
   if (P.seg1 < P.N && (P.seg1 % 256 || (P.seg2 - P.seg1) % 256)) return 128;
   if (P.seg2 < P.N && (P.N - P.seg2) % 256) return 128;
@@ -674,9 +675,16 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   double best_t = 0.0;
   int splits = tc_choose_splits(tiles_for(wmax), nkb, P.M, P.N, wmax, plans.num_sms,
                                 plans.part_elems, &best_t);
-  if (P.swiglu) {  // narrower tiles spread the gate/up features over more SMs
-    for (int nt : {192, 128}) {
-      if (nt >= wmax || (P.N / 2) % (nt / 2)) continue;
+  // narrower tiles spread the features over more SMs and, above 128 rows,
+  // keep two TMEM accumulator buffers.  For up to 128 rows only the SwiGLU
+  // projection takes them: measured on GB300 at the Qwen3-8B shapes, the
+  // model's preference for narrower split-K tiles there (O, down) did not
+  // hold, the extra activation traffic costing more than the partials saved.
+  for (int nt : {192, 128}) {
+    {
+      if (!P.swiglu && P.M <= 128) continue;
+      if (nt >= wmax || (P.swiglu ? (P.N / 2) % (nt / 2) : (nt == 192 || P.N % nt))) continue;
+      if (!P.swiglu && (P.seg1 % nt || P.seg2 % nt)) continue;
       double t = 0.0;
       const int s = tc_choose_splits(tiles_for(nt), nkb, P.M, P.N, nt, plans.num_sms,
                                      plans.part_elems, &t);
