@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_stack",
-                    choices=["full_stack", "low_entropy", "one_layer", "two_layer"])
+                    choices=["full_stack", "low_entropy", "one_layer", "two_layer",
+                             "two_layer_long"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 

@@ -135,6 +135,10 @@ WORKLOADS = {
     "two_layer": Workload("two_layer", qwen3_layers(2), batch=8, window=16,
                           prefix=4096, masked=16, all_masked_start=True,
                           steps=256, seed=0, extra_pages=256),
+    # the low_entropy shapes with 2 layers, for profiler captures
+    "two_layer_long": Workload("two_layer_long", qwen3_layers(2), batch=8, window=32,
+                               prefix=32768, masked=32, all_masked_start=True,
+                               plant=True, steps=256, tau=2.0, seed=0, extra_pages=512),
     # low-entropy long context: prefix 32768, W=32, batch 8, planted
     # peaked next-token bias on a seeded counting sequence
     "low_entropy": Workload("low_entropy", QWEN3_8B, batch=8, window=32,
