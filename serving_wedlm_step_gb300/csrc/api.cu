@@ -199,6 +199,66 @@ AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
   return A;
 }
 
+// The four projections of layer l on workspace activations (M rows).
+GemmProblem qkv_problem(wedlm_ctx* c, int l, int M, void* kv_win_layer) {
+  const wedlm_config& g = c->cfg;
+  const LayerWeights& w = c->layers[l];
+  const int nq = g.n_q_heads, nkv = g.n_kv_heads, hd = g.head_dim;
+  GemmProblem P{};
+  P.M = M; P.N = (nq + 2 * nkv) * hd; P.K = g.hidden; P.X = c->xn;
+  P.A0 = w.w_q; P.A1 = w.w_k; P.A2 = w.w_v;
+  P.seg1 = nq * hd; P.seg2 = (nq + nkv) * hd; P.swiglu = 0;
+  GemmEpi& e = P.epi;
+  e.mode = EPI_QKV; e.q_out = c->q; e.kv_win = kv_win_layer;
+  e.cosb = c->cosb; e.sinb = c->sinb; e.q_norm = w.q_norm; e.k_norm = w.k_norm;
+  e.qk_norm = g.qk_norm; e.W = g.window; e.Wp = c->Wp; e.nq = nq; e.nkv = nkv;
+  e.hd = hd; e.eps = g.rms_eps;
+  return P;
+}
+GemmProblem o_problem(wedlm_ctx* c, int l, int M, void* x, bool fuse) {
+  const wedlm_config& g = c->cfg;
+  const LayerWeights& w = c->layers[l];
+  GemmProblem P{};
+  P.M = M; P.N = g.hidden; P.K = g.n_q_heads * g.head_dim; P.X = c->o;
+  P.A0 = w.w_o; P.A1 = w.w_o; P.A2 = w.w_o; P.seg1 = P.N; P.seg2 = P.N;
+  P.epi.mode = EPI_RESID; P.epi.x = x;
+  if (fuse) {  // residual add + the FFN norm in one epilogue
+    P.epi.norm_w = w.ffn_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
+  }
+  return P;
+}
+GemmProblem gateup_problem(wedlm_ctx* c, int l, int M) {
+  const wedlm_config& g = c->cfg;
+  const LayerWeights& w = c->layers[l];
+  GemmProblem P{};
+  P.M = M; P.N = 2 * g.ffn; P.K = g.hidden; P.X = c->xn;
+  P.A0 = w.w_gate; P.A1 = w.w_up; P.A2 = w.w_up; P.seg1 = P.N; P.seg2 = P.N;
+  P.swiglu = 1;
+  P.epi.mode = EPI_SWIGLU; P.epi.act = c->act;
+  return P;
+}
+GemmProblem down_problem(wedlm_ctx* c, int l, int M, void* x, const void* next_norm) {
+  const wedlm_config& g = c->cfg;
+  const LayerWeights& w = c->layers[l];
+  GemmProblem P{};
+  P.M = M; P.N = g.hidden; P.K = g.ffn; P.X = c->act;
+  P.A0 = w.w_down; P.A1 = w.w_down; P.A2 = w.w_down; P.seg1 = P.N; P.seg2 = P.N;
+  P.epi.mode = EPI_RESID; P.epi.x = x;
+  if (next_norm) {
+    P.epi.norm_w = next_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
+  }
+  return P;
+}
+GemmProblem lmhead_problem(wedlm_ctx* c, int M) {
+  const wedlm_config& g = c->cfg;
+  GemmProblem P{};
+  P.M = M; P.N = g.vocab; P.K = g.hidden; P.X = c->xn;
+  P.A0 = c->lm_head; P.A1 = c->lm_head; P.A2 = c->lm_head;
+  P.seg1 = g.vocab; P.seg2 = g.vocab;
+  P.epi.mode = EPI_LMHEAD;
+  return P;
+}
+
 // rows a2..a4 for one layer, on workspace activations.  xn_ready: xn
 // already holds RMSNorm(x) with this layer's attention norm (written by the
 // previous layer's down projection); next_norm: when set, the down
@@ -212,25 +272,17 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
                const void* next_norm = nullptr) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
-  const int M = B * g.window, H = g.hidden, hd = g.head_dim;
-  const int nq = g.n_q_heads, nkv = g.n_kv_heads;
+  const int M = B * g.window, H = g.hidden;
   const bool fuse = g.dtype == WEDLM_BF16;
   int rc;
+  GemmProblem Pqkv = qkv_problem(c, l, M, kv_win_layer);
+  GemmProblem Po = o_problem(c, l, M, x, fuse);
+  GemmProblem Pgu = gateup_problem(c, l, M);
+  GemmProblem Pd = down_problem(c, l, M, x, fuse ? next_norm : nullptr);
   if (!xn_ready)
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
-  {
-    GemmProblem P{};
-    P.M = M; P.N = (nq + 2 * nkv) * hd; P.K = H; P.X = c->xn;
-    P.A0 = w.w_q; P.A1 = w.w_k; P.A2 = w.w_v;
-    P.seg1 = nq * hd; P.seg2 = (nq + nkv) * hd; P.swiglu = 0;
-    GemmEpi& e = P.epi;
-    e.mode = EPI_QKV; e.q_out = c->q; e.kv_win = kv_win_layer;
-    e.cosb = c->cosb; e.sinb = c->sinb; e.q_norm = w.q_norm; e.k_norm = w.k_norm;
-    e.qk_norm = g.qk_norm; e.W = g.window; e.Wp = c->Wp; e.nq = nq; e.nkv = nkv;
-    e.hd = hd; e.eps = g.rms_eps;
-    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_QKV, st))) return rc;
-  }
+  if ((rc = run_gemm<T>(c, Pqkv, WEDLM_KIND_GEMM_QKV, st))) return rc;
   AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
                          kv_win_layer, c->o);
   if (g.dtype == WEDLM_BF16) {
@@ -240,37 +292,12 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
     LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
     LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
   }
-  {
-    GemmProblem P{};
-    P.M = M; P.N = H; P.K = nq * hd; P.X = c->o;
-    P.A0 = w.w_o; P.A1 = w.w_o; P.A2 = w.w_o; P.seg1 = H; P.seg2 = H;
-    P.epi.mode = EPI_RESID; P.epi.x = x;
-    if (fuse) {  // residual add + the FFN norm in one epilogue
-      P.epi.norm_w = w.ffn_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
-    }
-    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_O, st))) return rc;
-  }
+  if ((rc = run_gemm<T>(c, Po, WEDLM_KIND_GEMM_O, st))) return rc;
   if (!fuse)
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, H, x, (const T*)w.ffn_norm, g.rms_eps, (T*)c->xn, st));
-  {
-    GemmProblem P{};
-    P.M = M; P.N = 2 * g.ffn; P.K = H; P.X = c->xn;
-    P.A0 = w.w_gate; P.A1 = w.w_up; P.A2 = w.w_up; P.seg1 = P.N; P.seg2 = P.N;
-    P.swiglu = 1;
-    P.epi.mode = EPI_SWIGLU; P.epi.act = c->act;
-    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_GATEUP, st))) return rc;
-  }
-  {
-    GemmProblem P{};
-    P.M = M; P.N = H; P.K = g.ffn; P.X = c->act;
-    P.A0 = w.w_down; P.A1 = w.w_down; P.A2 = w.w_down; P.seg1 = H; P.seg2 = H;
-    P.epi.mode = EPI_RESID; P.epi.x = x;
-    if (fuse && next_norm) {
-      P.epi.norm_w = next_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
-    }
-    if ((rc = run_gemm<T>(c, P, WEDLM_KIND_GEMM_DOWN, st))) return rc;
-  }
+  if ((rc = run_gemm<T>(c, Pgu, WEDLM_KIND_GEMM_GATEUP, st))) return rc;
+  if ((rc = run_gemm<T>(c, Pd, WEDLM_KIND_GEMM_DOWN, st))) return rc;
   return WEDLM_OK;
 }
 
@@ -285,12 +312,9 @@ int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant_phys,
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, g.hidden, x, (const T*)c->final_norm, g.rms_eps,
                              (T*)c->xn, st));
-  GemmProblem P{};
-  P.M = M; P.N = g.vocab; P.K = g.hidden; P.X = c->xn;
-  P.A0 = c->lm_head; P.A1 = c->lm_head; P.A2 = c->lm_head;
-  P.seg1 = g.vocab; P.seg2 = g.vocab;
+  GemmProblem P = lmhead_problem(c, M);
   GemmEpi& e = P.epi;
-  e.mode = EPI_LMHEAD; e.part = c->lm_part; e.mask_id = g.mask_id;
+  e.part = c->lm_part; e.mask_id = g.mask_id;
   e.vocab = g.vocab; e.plant = plant_phys; e.plant_bias = plant_bias;
   e.logits = logits;
   int tiles = 0;  // softmax records per row: one per output-feature tile

@@ -29,6 +29,13 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          int num_sms, size_t part_elems,
                                          std::string* msg);
 
+struct TcChoice {
+  bool cluster;  // split-K inside a thread-block cluster of `splits` blocks
+  int ntile;     // output features per tile
+  int splits;    // K splits
+};
+TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P);
+
 // Launches one GEMM; *tiles_out (may be null) receives the number of
 // output-feature tiles (the LM head's softmax records per row) and
 // *launches_out (may be null) the number of kernels enqueued (2 with split-K).

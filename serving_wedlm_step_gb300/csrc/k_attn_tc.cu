@@ -646,73 +646,74 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
           if (threadIdx.x == 0) s_merge = (atomicAdd(&A.unit_cnt[u], 1) == c1 - c0);
           softmax_bar();
           if (s_merge) {
-            // every segment of the unit is written: merge them into this
-            // thread's half row in slot order (the same sum whichever block
-            // merges) and reset the count for the next launch.  All loads of
-            // up to 4 segments are issued before they are used.
+            // every segment of the unit is written: merge them in slot
+            // order (the same sum whichever block merges) and reset the
+            // count for the next launch.  The 8 softmax warps split the
+            // unit into (32 rows, 32 dims) tasks; the (max, sum) and the
+            // partial O of two segments are loaded in one round trip, and
+            // the running result is rescaled when a pair raises the max.
             __threadfence();
-            if (valid) {
-              const int ns = c1 - c0 + 1;
-              const size_t s0 = (size_t)u + c0;
-              float M = -INFINITY, ls = 0.f;
-              float mk[4], lk[4];  // (max, sum) of up to 4 segments
-              for (int sb0 = 0; sb0 < ns; sb0 += 4) {
+            const int ns = c1 - c0 + 1;
+            const size_t s0 = (size_t)u + c0;
+            const int nrg = (R + 31) / 32;
+            for (int task = warp; task < nrg * 4; task += 8) {
+              const int mr = 32 * (task % nrg) + lane, qd = task / nrg;
+              if (mr >= R) continue;
+              const int hh = qd >> 1, d40 = (qd & 1) * 8;
+              float M = -INFINITY, ls = 0.f, acc[32];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              for (int sb0 = 0; sb0 < ns; sb0 += 2) {
+                float mk[2], lk[2];
+                float4 t4[2][8];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
                   mk[k] = -INFINITY;
                   lk[k] = 0.f;
                   if (sb0 + k < ns) {
-                    const size_t row = (s0 + sb0 + k) * R + r;
-                    mk[k] = __ldcg(A.part_ml + row * 2);
-                    lk[k] = __ldcg(A.part_ml + row * 2 + 1);
+                    const size_t sid = s0 + sb0 + k;
+                    mk[k] = __ldcg(A.part_ml + (sid * R + mr) * 2);
+                    lk[k] = __ldcg(A.part_ml + (sid * R + mr) * 2 + 1);
+                    const float4* src = reinterpret_cast<const float4*>(A.part_o) +
+                                        ((sid * 2 + hh) * 16 + d40) * R + mr;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) t4[k][j] = __ldcg(src + (size_t)j * R);
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) t4[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
                   }
                 }
+                const float Mn = fmaxf(M, fmaxf(mk[0], mk[1]));
+                if (Mn == -INFINITY) continue;  // no key seen yet for this row
+                if (Mn != M) {
+                  const float a = exp2f(M - Mn);  // 0 while M is -inf
+                  ls *= a;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) M = fmaxf(M, mk[k]);
-              }
-#pragma unroll
-              for (int j = 0; j < 64; ++j) o[j] = 0.f;
-              for (int sb0 = 0; sb0 < ns; sb0 += 4) {
-                if (ns > 4) {  // several chunks: the first pass left the last one loaded
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    mk[k] = -INFINITY;
-                    lk[k] = 0.f;
-                    if (sb0 + k < ns) {
-                      const size_t row = (s0 + sb0 + k) * R + r;
-                      mk[k] = __ldcg(A.part_ml + row * 2);
-                      lk[k] = __ldcg(A.part_ml + row * 2 + 1);
-                    }
-                  }
+                  for (int j = 0; j < 32; ++j) acc[j] *= a;
+                  M = Mn;
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const int sg = sb0 + k;
-                  if (sg >= ns || mk[k] == -INFINITY) continue;
+                for (int k = 0; k < 2; ++k) {
+                  if (mk[k] == -INFINITY) continue;
                   const float wgt = exp2f(mk[k] - M);
                   ls += lk[k] * wgt;
-                  const float4* src =
-                      reinterpret_cast<const float4*>(A.part_o) + ((s0 + sg) * 2 + h) * 16 * R + r;
-                  float4 t4[16];
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) t4[j] = __ldcg(src + (size_t)j * R);
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    o[4 * j] += t4[j].x * wgt; o[4 * j + 1] += t4[j].y * wgt;
-                    o[4 * j + 2] += t4[j].z * wgt; o[4 * j + 3] += t4[j].w * wgt;
+                  for (int j = 0; j < 8; ++j) {
+                    acc[4 * j] += t4[k][j].x * wgt; acc[4 * j + 1] += t4[k][j].y * wgt;
+                    acc[4 * j + 2] += t4[k][j].z * wgt; acc[4 * j + 3] += t4[k][j].w * wgt;
                   }
                 }
               }
               const float inv = ls > 0.f ? 1.f / ls : 0.f;
               bf16* dst = static_cast<bf16*>(A.o) +
-                          ((size_t)(b * W + p_row) * A.nq + kvh * G + r % G) * hd + h * 64;
+                          ((size_t)(b * W + mr / G) * A.nq + kvh * G + mr % G) * hd + qd * 32;
 #pragma unroll
-              for (int j8 = 0; j8 < 8; ++j8) {
+              for (int j8 = 0; j8 < 4; ++j8) {
                 uint32_t w4[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const __nv_bfloat162 t2 =
-                      __floats2bfloat162_rn(o[8 * j8 + 2 * k] * inv, o[8 * j8 + 2 * k + 1] * inv);
+                  const __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[8 * j8 + 2 * k] * inv,
+                                                                  acc[8 * j8 + 2 * k + 1] * inv);
                   w4[k] = *reinterpret_cast<const uint32_t*>(&t2);
                 }
                 reinterpret_cast<uint4*>(dst)[j8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);

@@ -69,7 +69,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
 struct TcLaunch {
   int stages, ntile, nrb, nbuf, tiles;
   uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
+  uint32_t stg_off;  // split-K partials: 4 KB staging box per epilogue warp
 };
+constexpr uint32_t kStageBoxBytes = 32 * 32 * 4;  // 32 rows x 32 fp32 columns
 
 // kCluster: split-K inside a thread-block cluster of P.splits blocks (one
 // unit per block, cluster rank = split); the splits are added through
@@ -78,7 +80,7 @@ template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mX,
-               GemmProblem P, TcLaunch L) {
+               const __grid_constant__ CUtensorMap mPart, GemmProblem P, TcLaunch L) {
   extern __shared__ uint8_t dsm_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
@@ -236,17 +238,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
         } else if (kCluster) {
           // the accumulator stays in TMEM for the exchange below
-        } else {
-          float* dst = P.partial + (size_t)split * P.M * P.N + (size_t)m * P.N + tile * ntile;
-          for (int c = 0; c < ntile; c += 32) {
+        } else if (r * 128 + 32 * q < P.M) {
+          // fp32 partial [split][M][N]: the warp's 32 rows x 32 columns go
+          // to its staging box in the 128-byte swizzle (16-byte chunk j of
+          // row i at chunk j ^ (i % 8): the row-per-lane writes hit every
+          // bank once per 8 lanes) and one lane stores the box with TMA,
+          // whole 128-byte rows; rows and columns outside [M][N] are clipped
+          const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+          for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
             float v[32];
             tmem_ld32(taddr + (uint32_t)c, v);
-            if (m < P.M) {
+            if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+            __syncwarp();
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (tile * ntile + c + 4 * i < P.N)
-                  __stcg(reinterpret_cast<float4*>(dst + c) + i,
-                         make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            for (int j = 0; j < 8; ++j)
+              st_shared_f32x4(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), v[4 * j],
+                              v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&mPart, stg, tile * ntile + c, r * 128 + 32 * q, split);
+              bulk_commit();
             }
           }
         }
@@ -255,6 +267,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);  // accumulator free for the MMA warp
     }
+    if (lane == 0) bulk_wait0();  // partials written before the block exits
   }
   if constexpr (kCluster) {
     // Row group g (TMEM lanes 32g..32g+31) of the tile belongs to cluster
@@ -523,6 +536,21 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint3
   return r == CUDA_SUCCESS;
 }
 
+// split-K partials [S][M][N] fp32 as a 3-D tensor for TMA stores of
+// 32 x 32 boxes, 128-byte swizzle (one box row = 32 floats = 128 bytes)
+bool encode_partial(CUtensorMap* m, void* ptr, uint64_t N, uint64_t M, uint64_t S) {
+  auto enc = get_encode();
+  if (!enc || (N * 4) % 16) return false;
+  cuuint64_t dims[3] = {N, M, S};
+  cuuint64_t strides[2] = {N * 4, M * N * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // weight descriptors for boxes of 64, 96, 128 and 256 rows (x 64 K
@@ -654,47 +682,46 @@ int tc_tile_width(const GemmProblem& P) {
   return 256;
 }
 
-cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cudaStream_t st,
-                           int* tiles_out, int* launches_out) {
-  (void)kind;
-  if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
+namespace {
+int tc_tiles_for(const GemmProblem& P, int ntile) {
+  return P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
+}
+}  // namespace
+
+// The plan of one GEMM: the persistent kernel (split-K through global
+// partials when splits > 1) or split-K inside clusters of S blocks.
+// Clusters serve the per-head QKV epilogue of one 128-row block of
+// activations: there they beat the global partials (measured 29 vs 34 us for
+// the Qwen3-8B shape); the residual epilogues keep the persistent path,
+// whose split-K epilogue also fuses the next RMSNorm.  Modelled like
+// tc_choose_splits (one wave of clusters, about 2 us for the exchange).
+TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P) {
   const int nkb = P.K / kBK;
   const int wmax = tc_tile_width(P);
-  auto tiles_for = [&](int ntile) {
-    return P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
-  };
-  // the plan: the persistent kernel (split-K through global partials when
-  // splits > 1) or split-K inside clusters of S blocks.  Clusters serve the
-  // per-head QKV epilogue of one 128-row block of activations: there they
-  // beat the global partials (measured 29 vs 34 us for the Qwen3-8B shape);
-  // the residual epilogues keep the persistent path, whose split-K
-  // epilogue also fuses the next RMSNorm.  Modelled like tc_choose_splits
-  // (one wave of clusters, about 2 us for the exchange).
-  bool cluster = false;
-  int ntile = wmax;
+  TcChoice c;
+  c.cluster = false;
+  c.ntile = wmax;
   double best_t = 0.0;
-  int splits = tc_choose_splits(tiles_for(wmax), nkb, P.M, P.N, wmax, plans.num_sms,
-                                plans.part_elems, &best_t);
+  c.splits = tc_choose_splits(tc_tiles_for(P, wmax), nkb, P.M, P.N, wmax, plans.num_sms,
+                              plans.part_elems, &best_t);
   // narrower tiles spread the features over more SMs and, above 128 rows,
   // keep two TMEM accumulator buffers.  For up to 128 rows only the SwiGLU
   // projection takes them: measured on GB300 at the Qwen3-8B shapes, the
   // model's preference for narrower split-K tiles there (O, down) did not
   // hold, the extra activation traffic costing more than the partials saved.
   for (int nt : {192, 128}) {
-    {
-      if (!P.swiglu && P.M <= 128) continue;
-      if (nt >= wmax || (P.swiglu ? (P.N / 2) % (nt / 2) : (nt == 192 || P.N % nt))) continue;
-      if (!P.swiglu && (P.seg1 % nt || P.seg2 % nt)) continue;
-      double t = 0.0;
-      const int s = tc_choose_splits(tiles_for(nt), nkb, P.M, P.N, nt, plans.num_sms,
-                                     plans.part_elems, &t);
-      if (t < best_t * (1.0 - 1e-9)) { best_t = t; ntile = nt; splits = s; }
-    }
+    if (!P.swiglu && P.M <= 128) continue;
+    if (nt >= wmax || (P.swiglu ? (P.N / 2) % (nt / 2) : (nt == 192 || P.N % nt))) continue;
+    if (!P.swiglu && (P.seg1 % nt || P.seg2 % nt)) continue;
+    double t = 0.0;
+    const int s = tc_choose_splits(tc_tiles_for(P, nt), nkb, P.M, P.N, nt, plans.num_sms,
+                                   plans.part_elems, &t);
+    if (t < best_t * (1.0 - 1e-9)) { best_t = t; c.ntile = nt; c.splits = s; }
   }
   if (P.M <= 128 && P.epi.mode == EPI_QKV) {
     for (int nt = wmax; nt >= 128; nt /= 2) {
       if (nt != wmax && (P.swiglu || P.N % nt)) break;
-      const int tiles = tiles_for(nt);
+      const int tiles = tc_tiles_for(P, nt);
       const double w_kb = (double)nt * kBK * 2, t_all = (double)tiles * nkb * w_kb / 6.5e12;
       for (int S = 2; S <= kMaxCluster; ++S) {
         if (nkb / S < 4 || tiles > plans.max_clusters[S] ||
@@ -702,10 +729,26 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
           continue;
         const int kper = (nkb + S - 1) / S;
         const double t = std::max(kper * (w_kb + kXBlockBytes) / 65e9, t_all) + 2e-6;
-        if (t < best_t * (1.0 - 1e-9)) { best_t = t; cluster = true; ntile = nt; splits = S; }
+        if (t < best_t * (1.0 - 1e-9)) {
+          best_t = t;
+          c.cluster = true;
+          c.ntile = nt;
+          c.splits = S;
+        }
       }
     }
   }
+  return c;
+}
+
+cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cudaStream_t st,
+                           int* tiles_out, int* launches_out) {
+  (void)kind;
+  if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
+  const TcChoice choice = tc_plan(plans, P);
+  const bool cluster = choice.cluster;
+  const int ntile = choice.ntile, splits = choice.splits;
+  auto tiles_for = [&](int nt) { return tc_tiles_for(P, nt); };
   const int bslot = box_slot(P.swiglu ? ntile / 2 : ntile);
   if (bslot < 0) return cudaErrorInvalidValue;
   auto find = [&](const void* w) -> const CUtensorMap* {
@@ -723,14 +766,24 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   L.nbuf = L.buf_cols * 2 <= 512 ? 2 : 1;
   L.a_bytes = (uint32_t)L.nrb * kXBlockBytes;
   L.stage_bytes = L.a_bytes + (uint32_t)L.ntile * 128u;
-  L.stages = (int)std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024) / L.stage_bytes);
+  // persistent split-K: 4 staging boxes for the partial stores after the ring
+  const uint32_t stg_bytes = (!cluster && splits > 1) ? 4 * kStageBoxBytes : 0;
+  L.stages = (int)std::min<uint32_t>(kMaxStages,
+                                     (kMaxDynSmem - 1024 - stg_bytes) / L.stage_bytes);
   if (L.stages < 2) return cudaErrorInvalidValue;
+  L.stg_off = (uint32_t)L.stages * L.stage_bytes;  // a multiple of 1024
   uint32_t cols = 32;
   while (cols < L.buf_cols * (uint32_t)L.nbuf) cols <<= 1;
   if (cols > 512) return cudaErrorInvalidValue;
   L.tmem_cols = cols;
-  CUtensorMap mx;
+  CUtensorMap mx, mpart;
   if (!encode_2d(&mx, P.X, P.K, P.M, 128)) return cudaErrorInvalidValue;
+  if (stg_bytes) {
+    if (!P.partial || !encode_partial(&mpart, P.partial, P.N, P.M, splits))
+      return cudaErrorInvalidValue;
+  } else {
+    mpart = mx;  // not read
+  }
   L.tiles = tiles_for(ntile);
   if (tiles_out) *tiles_out = L.tiles;
   P.splits = splits;
@@ -753,7 +806,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, *a0, *a1, *a2, mx, P, L);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, *a0, *a1, *a2, mx, mpart, P, L);
     if (launches_out) *launches_out = norm ? 2 : 1;
     if (e != cudaSuccess) return e;
     if (norm)
@@ -763,9 +816,9 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
     return cudaGetLastError();
   }
   const int grid = std::min(units, plans.num_sms);
-  const size_t smem = (size_t)L.stages * L.stage_bytes + 1024;
+  const size_t smem = (size_t)L.stages * L.stage_bytes + stg_bytes + 1024;
   cudaError_t le = launch_pdl(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, st, *a0, *a1,
-                              *a2, mx, P, L);
+                              *a2, mx, mpart, P, L);
   if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
   if (le != cudaSuccess) return le;
   if (P.splits == 1 && norm) {
