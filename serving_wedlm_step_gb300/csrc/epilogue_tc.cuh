@@ -16,13 +16,11 @@
 namespace wedlm {
 
 // where one thread's accumulator row comes from
-enum AccFrom { ACC_PARTIAL = 0, ACC_TMEM = 1, ACC_SMEM = 2 };
+enum AccFrom { ACC_PARTIAL = 0, ACC_TMEM = 1 };
 struct AccRow {
   int from;             // AccFrom (warp-uniform)
   uint32_t taddr;       // ACC_TMEM: TMEM address of column 0 (this warp's lanes)
-  const float* part;    // ACC_PARTIAL: partial[0][m][tile*ntile] (global);
-                        // ACC_SMEM: this row in the first contribution (shared,
-                        // [column][32 rows]: column c at part[c * 32])
+  const float* part;    // ACC_PARTIAL: partial[0][m][tile*ntile] (global)
   size_t split_stride;  // floats from one split's row to the next split's
   int splits;
   int col0;             // tile * ntile (first global column of the tile)
@@ -41,14 +39,6 @@ __device__ __forceinline__ void acc_chunk(const AccRow& a, int c, float (&v)[32]
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = 0.f;
   if (!a.valid) return;
-  if (a.from == ACC_SMEM) {  // the splits' contributions, summed in split order
-    for (int sp = 0; sp < a.splits; ++sp) {
-      const float* p = a.part + (size_t)sp * a.split_stride + (size_t)c * 32;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += p[j * 32];
-    }
-    return;
-  }
   for (int sp = 0; sp < a.splits; ++sp) {
     const float* p = a.part + (size_t)sp * a.split_stride + c;
 #pragma unroll

@@ -14,7 +14,6 @@ struct TcMapTable;  // TMA descriptors of every weight matrix
 // Everything the bf16 GEMMs need that is fixed at create time.
 struct TcPlanSet {
   int num_sms = 0;
-  int max_clusters[9] = {};  // clusters of S blocks (index S <= 8) resident at once
   size_t part_elems = 0;
   std::shared_ptr<TcMapTable> maps;
 };
@@ -30,7 +29,6 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
                                          std::string* msg);
 
 struct TcChoice {
-  bool cluster;  // split-K inside a thread-block cluster of `splits` blocks
   int ntile;     // output features per tile
   int splits;    // K splits
 };

@@ -7,17 +7,18 @@
 // side.  Persistent, warp-specialised: one block per SM loops over work
 // units;
 //   warp 0 / lane 0: TMA producer.  Each pipeline stage is one 64-wide K
-//       slice: the activation row blocks and the tile's weight rows (boxes
-//       of 64 rows, L2 evict-first), 128-byte swizzle, in a ring of
-//       shared-memory stages guarded by full/empty mbarriers;
+//       slice: the activation row blocks and the tile's weight rows (one
+//       box per tile, two for SwiGLU; L2 evict-first), 128-byte swizzle, in
+//       a ring of shared-memory stages guarded by full/empty mbarriers;
 //   warp 1 / lane 0: MMA issuer: 4 x tcgen05.mma (K = 16) per stage and
 //       row block into one of two TMEM accumulators; a tcgen05.commit frees
 //       each stage, another hands the finished accumulator to the epilogue;
 //   warps 2-5: epilogue, one activation row per thread (TMEM lane quadrant
 //       = warp % 4), straight from TMEM (epilogue_tc.cuh), overlapping the
-//       next unit's mainloop.  With split-K they store the fp32 partial;
-//       a split-K epilogue kernel then sums the partials in split order,
-//       consecutive threads on consecutive columns, and runs the epilogue.
+//       next unit's mainloop.  With split-K they store the fp32 partial
+//       (32 x 32 boxes staged in shared memory, written by TMA); a split-K
+//       epilogue kernel then sums the partials in split order, consecutive
+//       threads on consecutive columns, and runs the epilogue.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -34,7 +35,6 @@ constexpr int kBK = 64;                           // K elements per stage (128 b
 constexpr uint32_t kXBlockBytes = 128 * kBK * 2;  // one activation row block
 constexpr int kThreads = 192;                     // producer, MMA, 4 epilogue warps
 constexpr int kMaxDynSmem = 221 * 1024;
-constexpr int kMaxCluster = 8;                    // portable cluster sizes
 
 __device__ __forceinline__ void epi_bar() {       // the 4 epilogue warps only
   asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -50,22 +50,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 }
 }  // namespace
 
-// all threads of all blocks of the cluster (release / acquire)
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// address of the same shared-memory location in block `rank` of the cluster
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
-}
-
 struct TcLaunch {
   int stages, ntile, nrb, nbuf, tiles;
   uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
@@ -73,10 +57,6 @@ struct TcLaunch {
 };
 constexpr uint32_t kStageBoxBytes = 32 * 32 * 4;  // 32 rows x 32 fp32 columns
 
-// kCluster: split-K inside a thread-block cluster of P.splits blocks (one
-// unit per block, cluster rank = split); the splits are added through
-// distributed shared memory instead of global partials.
-template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mX,
@@ -236,8 +216,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         if (P.splits == 1) {
           AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
-        } else if (kCluster) {
-          // the accumulator stays in TMEM for the exchange below
         } else if (r * 128 + 32 * q < P.M) {
           // fp32 partial [split][M][N]: the warp's 32 rows x 32 columns go
           // to its staging box in the 128-byte swizzle (16-byte chunk j of
@@ -268,45 +246,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       if (lane == 0) mbar_arrive(&acc_empty[buf]);  // accumulator free for the MMA warp
     }
     if (lane == 0) bulk_wait0();  // partials written before the block exits
-  }
-  if constexpr (kCluster) {
-    // Row group g (TMEM lanes 32g..32g+31) of the tile belongs to cluster
-    // rank g % S.  Every block sends its rows of each group to the group's
-    // owner, column by column ([column][32 rows]: each warp store is 128
-    // contiguous bytes); the owner adds the S contributions in rank order
-    // and runs the epilogue on its rows, 4 warps splitting the epilogue items.
-    const int S = P.splits, rank = (int)(blockIdx.x % S), tile = (int)(blockIdx.x / S);
-    const int grp = 32 * ntile;             // floats of one group contribution
-    tc_fence_before();
-    __syncwarp();
-    cluster_sync();  // every block's main loop is done: shared memory is free
-    tc_fence_after();
-    if (warp >= 2) {
-      const int g = warp & 3, owner = g % S, lg = g / S;
-      const uint32_t local = smem_u32(base) + (uint32_t)(((lg * S + rank) * grp + lane) * 4);
-      const uint32_t remote = cluster_addr(local, (uint32_t)owner);
-      const uint32_t taddr = tmem + ((uint32_t)(32 * g) << 16);
-      for (int c = 0; c < ntile; c += 32) {
-        float v[32];
-        tmem_ld32(taddr + (uint32_t)c, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) st_cluster_f32(remote + (uint32_t)((c + j) * 128), v[j]);
-      }
-    }
-    tc_fence_before();
-    __syncwarp();
-    cluster_sync();  // every contribution has landed
-    tc_fence_after();
-    if (warp >= 2) {
-      const int items = tc_epi_items(P, ntile);
-      for (int lg = 0; rank + lg * S < 4; ++lg) {
-        const int m = 32 * (rank + lg * S) + lane;
-        const float* part = reinterpret_cast<const float*>(base) + (size_t)(lg * S) * grp + lane;
-        AccRow a{ACC_SMEM, 0, part, (size_t)grp, S, tile * ntile, P.N, m < P.M};
-        for (int it = warp - 2; it < items; it += 4)
-          tc_epilogue_rows(P, a, m, tile, ntile, it, it + 1);
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -605,35 +544,12 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
     return nullptr;
   }
   // dynamic shared memory: up to 220 KB of stages + 1 KB alignment slack
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxDynSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxDynSmem);
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (msg) *msg = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return nullptr;
-  }
-  // clusters of S blocks that fit on the GPU at once (0: none)
-  for (int S = 2; S <= kMaxCluster; ++S) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S * 64);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kMaxDynSmem;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = S;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<true>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-    p->max_clusters[S] = n;
   }
   return p;
 }
@@ -664,12 +580,6 @@ int tc_choose_splits(int tiles, int nkb, int M, int N, int ntile, int num_sms,
   return best;
 }
 
-// shared memory one block of a cluster needs for the split-K exchange: the
-// rank-0 block owns ceil(4 / S) row groups, each S contributions of 32 rows
-size_t tc_cluster_xbytes(int S, int ntile) {
-  return (size_t)((4 + S - 1) / S) * S * 32 * ntile * 4;
-}
-
 // widest tile of output features: 256 while the 128-row activation blocks
 // fit one 256-column TMEM accumulator each (up to 256 rows; one accumulator
 // buffer instead of two above 128 rows), else 128; every segment boundary
@@ -688,18 +598,13 @@ int tc_tiles_for(const GemmProblem& P, int ntile) {
 }
 }  // namespace
 
-// The plan of one GEMM: the persistent kernel (split-K through global
-// partials when splits > 1) or split-K inside clusters of S blocks.
-// Clusters serve the per-head QKV epilogue of one 128-row block of
-// activations: there they beat the global partials (measured 29 vs 34 us for
-// the Qwen3-8B shape); the residual epilogues keep the persistent path,
-// whose split-K epilogue also fuses the next RMSNorm.  Modelled like
-// tc_choose_splits (one wave of clusters, about 2 us for the exchange).
+// The plan of one GEMM: tile width and split-K factor of the persistent
+// kernel (split-K through fp32 partials and an epilogue kernel when
+// splits > 1).
 TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P) {
   const int nkb = P.K / kBK;
   const int wmax = tc_tile_width(P);
   TcChoice c;
-  c.cluster = false;
   c.ntile = wmax;
   double best_t = 0.0;
   c.splits = tc_choose_splits(tc_tiles_for(P, wmax), nkb, P.M, P.N, wmax, plans.num_sms,
@@ -718,26 +623,6 @@ TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P) {
                                    plans.part_elems, &t);
     if (t < best_t * (1.0 - 1e-9)) { best_t = t; c.ntile = nt; c.splits = s; }
   }
-  if (P.M <= 128 && P.epi.mode == EPI_QKV) {
-    for (int nt = wmax; nt >= 128; nt /= 2) {
-      if (nt != wmax && (P.swiglu || P.N % nt)) break;
-      const int tiles = tc_tiles_for(P, nt);
-      const double w_kb = (double)nt * kBK * 2, t_all = (double)tiles * nkb * w_kb / 6.5e12;
-      for (int S = 2; S <= kMaxCluster; ++S) {
-        if (nkb / S < 4 || tiles > plans.max_clusters[S] ||
-            tc_cluster_xbytes(S, nt) > (size_t)kMaxDynSmem - 1024)
-          continue;
-        const int kper = (nkb + S - 1) / S;
-        const double t = std::max(kper * (w_kb + kXBlockBytes) / 65e9, t_all) + 2e-6;
-        if (t < best_t * (1.0 - 1e-9)) {
-          best_t = t;
-          c.cluster = true;
-          c.ntile = nt;
-          c.splits = S;
-        }
-      }
-    }
-  }
   return c;
 }
 
@@ -746,7 +631,6 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
   const TcChoice choice = tc_plan(plans, P);
-  const bool cluster = choice.cluster;
   const int ntile = choice.ntile, splits = choice.splits;
   auto tiles_for = [&](int nt) { return tc_tiles_for(P, nt); };
   const int bslot = box_slot(P.swiglu ? ntile / 2 : ntile);
@@ -767,7 +651,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   L.a_bytes = (uint32_t)L.nrb * kXBlockBytes;
   L.stage_bytes = L.a_bytes + (uint32_t)L.ntile * 128u;
   // persistent split-K: 4 staging boxes for the partial stores after the ring
-  const uint32_t stg_bytes = (!cluster && splits > 1) ? 4 * kStageBoxBytes : 0;
+  const uint32_t stg_bytes = splits > 1 ? 4 * kStageBoxBytes : 0;
   L.stages = (int)std::min<uint32_t>(kMaxStages,
                                      (kMaxDynSmem - 1024 - stg_bytes) / L.stage_bytes);
   if (L.stages < 2) return cudaErrorInvalidValue;
@@ -789,35 +673,9 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   P.splits = splits;
   const int units = L.tiles * P.splits;
   const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
-  if (cluster) {
-    size_t smem = (size_t)L.stages * L.stage_bytes;
-    smem = std::max(smem, tc_cluster_xbytes(P.splits, ntile)) + 1024;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(units);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute at[2];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = P.splits;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true>, *a0, *a1, *a2, mx, mpart, P, L);
-    if (launches_out) *launches_out = norm ? 2 : 1;
-    if (e != cudaSuccess) return e;
-    if (norm)
-      return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
-                                  static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
-                                  static_cast<bf16*>(P.epi.xn), st);
-    return cudaGetLastError();
-  }
   const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + stg_bytes + 1024;
-  cudaError_t le = launch_pdl(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, st, *a0, *a1,
+  cudaError_t le = launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, st, *a0, *a1,
                               *a2, mx, mpart, P, L);
   if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
   if (le != cudaSuccess) return le;
