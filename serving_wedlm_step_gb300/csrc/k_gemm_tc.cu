@@ -36,10 +36,6 @@ constexpr uint32_t kXBlockBytes = 128 * kBK * 2;  // one activation row block
 constexpr int kThreads = 192;                     // producer, MMA, 4 epilogue warps
 constexpr int kMaxDynSmem = 221 * 1024;
 
-__device__ __forceinline__ void epi_bar() {       // the 4 epilogue warps only
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
 // bounded wait that gives up at once after any wait of this block timed out
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
                                               volatile int* abort) {
