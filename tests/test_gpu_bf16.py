@@ -157,22 +157,28 @@ def test_growing_scores_attention_matches_oracle():
     assert worst <= TOL
 
 
-def test_ragged_layer_matches_oracle(one_layer):
-    """The whole decoder layer at the ragged shape (B=32, 512 window rows),
+@pytest.mark.parametrize("B,W,prefix,seed,sample", [
+    (32, 16, (512, 8192), 3, (0, 7, 19, 31)),  # 512 rows: 4 row blocks, 128-wide tiles
+    (9, 16, (300, 3000), 4, (0, 4, 8)),        # 144 rows: 2 row blocks, ragged second
+    (5, 8, (100, 700), 5, (0, 2, 4)),          # 40 rows: one partly filled row block
+])
+def test_ragged_layer_matches_oracle(one_layer, B, W, prefix, seed, sample):
+    """The whole decoder layer at ragged shapes (row counts that are not
+    multiples of the 32-row partial boxes or of the 128-row MMA blocks),
     sampled sequences compared with the oracle layer on the same input."""
     s, w, w_np = one_layer
-    wl = Workload("ragged", s, batch=32, window=16, prefix=(512, 8192), masked=(4, 12),
-                  shuffled_pages=True, seed=3)
+    wl = Workload("ragged", s, batch=B, window=W, prefix=prefix, masked=(W // 4, 3 * W // 4),
+                  shuffled_pages=True, seed=seed)
     st = make_state_np(wl)
-    B, W = 32, 16
-    pool = make_pool_torch(s, st["num_pages"], 3, 0)
+    pool = make_pool_torch(s, st["num_pages"], seed, 0)
     ctx = _ctx(s, w, W, B, st["max_pages"])
     x = torch.empty(B * W, s.hidden, dtype=torch.bfloat16, device="cuda")
     pos_phys = torch.empty(B * W, dtype=torch.int32, device="cuda")
     perm = torch.empty(B, W, dtype=torch.int32, device="cuda")
     ctx.reorder_embed(dev(st["tokens"]), dev(st["pos"]), dev(st["obs"]), perm, None, x, pos_phys)
     x_in = x.float().cpu().numpy()
-    win = torch.empty(B, 2, s.n_kv_heads, 16 * s.head_dim, dtype=torch.bfloat16, device="cuda")
+    Wp = (W + 15) // 16 * 16  # the window rounded up to a page
+    win = torch.empty(B, 2, s.n_kv_heads, Wp * s.head_dim, dtype=torch.bfloat16, device="cuda")
     q_out = torch.empty(B * W, s.n_q_heads * s.head_dim, dtype=torch.bfloat16, device="cuda")
     a_out = torch.empty_like(q_out)
     ctx.layer(0, x, pos_phys, dev(st["seq_len"]), dev(st["page_table"]), st["num_pages"],
@@ -184,7 +190,7 @@ def test_ragged_layer_matches_oracle(one_layer):
     perm_np = perm.cpu().numpy()
     pool_f = pool_np(pool)
     store = O.storer("bf16")
-    for b in (0, 7, 19, 31):
+    for b in sample:
         p_ref, _ = O.topological_reorder(st["obs"][b])
         assert perm_np[b].tolist() == p_ref.tolist()
         assert pos_np[b * W:(b + 1) * W].tolist() == st["pos"][b][p_ref].tolist()
