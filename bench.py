@@ -331,6 +331,13 @@ def run_ours(args):
                 "unit": "GB/s", "frac": round(dk["gbs"] / hbm, 3), "traffic": traffic,
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": byts[dom]}
+    # the whole step against the HBM roofline: every kind's algorithmic bytes
+    # times its launches per step, at the measured copy bandwidth
+    step_bytes = sum(byts[k2] * kernels[k2]["launches"] / n_timing for k2 in kernels if k2 in byts)
+    t_roof_ms = step_bytes / (hbm * 1e9) * 1e3
+    step_roofline = {"bound": "hbm", "algorithmic_bytes": int(step_bytes),
+                     "t_roof_ms": round(t_roof_ms, 4), "peak": hbm, "unit": "GB/s",
+                     "frac": round(t_roof_ms / (ms / args.steps), 3)}
     launches = ctx.launches_per_step(B)
 
     res = {
@@ -355,6 +362,7 @@ def run_ours(args):
         "launches_per_step": launches,
         "clocks": clk,
         "roofline": roofline,
+        "step_roofline": step_roofline,
         "kernels": kernels,
     }
     if rank == 0 and not args.no_cpu_baseline:
