@@ -234,6 +234,52 @@ def window_attention(q, k_pre, v_pre, k_win, v_win, visible=None):
     return out
 
 
+def dual_stream_visibility(n, block):
+    """Visibility of Dual-Stream Masking over the 2n keys [memory stream ||
+    prediction stream] for the 2n query rows in the same order (Key claims
+    §4.2, Eq. 8-10; Method: "prediction-stream tokens in block i attend to
+    memory-stream tokens whose logical positions precede i").  Memory row r
+    (logical position r) sees memory keys 0..r.  Prediction row n+i lies in
+    block j = i // block at physical index p = i % block of the block's
+    topologically reordered order; it sees the memory keys at positions
+    before the block, 0..j*block-1, and the keys of its own block at physical
+    index <= p (causal in the reordered order)."""
+    vis = np.zeros((2 * n, 2 * n), bool)
+    for r in range(n):
+        vis[r, :r + 1] = True
+    for i in range(n):
+        j, p = divmod(i, block)
+        vis[n + i, :j * block] = True
+        vis[n + i, n + j * block:n + j * block + p + 1] = True
+    return vis
+
+
+def dual_stream_attention(q, k_mem, v_mem, k_pred, v_pred, block):
+    """Attention of both streams under Dual-Stream Masking.
+
+    q: [2n][nq][hd] (memory rows, then prediction rows); k/v of each stream:
+    [n][nkv][hd].  Softmax with scale 1/sqrt(hd) over the visible keys;
+    query head h reads kv head h // (nq/nkv).  Returns [2n][nq][hd]."""
+    q = np.asarray(q, np.float64)
+    n2, nq, hd = q.shape
+    n = n2 // 2
+    keys = np.concatenate([k_mem, k_pred], 0).astype(np.float64)
+    vals = np.concatenate([v_mem, v_pred], 0).astype(np.float64)
+    nkv = keys.shape[1]
+    group = nq // nkv
+    vis = dual_stream_visibility(n, block)
+    out = np.zeros((n2, nq, hd))
+    for h in range(nq):
+        g = h // group
+        s = (q[:, h] @ keys[:, g].T) / np.sqrt(hd)
+        s = np.where(vis, s, -np.inf)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h] = p @ vals[:, g]
+    return out
+
+
 def _f64(a):
     return np.asarray(a, np.float64)
 
@@ -258,16 +304,20 @@ def qkv_project(shape, lw, x, cos, sin, store):
     return xn, q, k, v
 
 
-def layer_forward(shape, lw, x, cos, sin, k_pre, v_pre, store, visible=None):
+def layer_forward(shape, lw, x, cos, sin, k_pre, v_pre, store, visible=None, mid=None):
     """One pre-norm decoder layer over the window rows.
 
-    Returns (x_out, k_win, v_win, attn_out).
+    Returns (x_out, k_win, v_win, attn_out).  When `mid` is a list, the
+    residual stream between the attention block and the FFN (as stored) is
+    appended to it.
     """
     s = shape
     W = x.shape[0]
     _, q, k, v = qkv_project(s, lw, x, cos, sin, store)
     o = store(window_attention(q, k_pre, v_pre, k, v, visible))
     x = store(x + o.reshape(W, -1) @ _f64(lw["w_o"]).T)
+    if mid is not None:
+        mid.append(x)
     xn = store(rmsnorm(x, lw["ffn_norm"], s.rms_eps))
     g = xn @ _f64(lw["w_gate"]).T
     u = xn @ _f64(lw["w_up"]).T
@@ -319,6 +369,22 @@ def softmax_scores(z):
 # ---------------------------------------------------------------------------
 # Eq. 11 selection and the commit / refill (Method)
 # ---------------------------------------------------------------------------
+
+
+SCORE_ENTROPY, SCORE_NEGLOGP = 0, 1
+
+
+def slot_score(scores, mode):
+    """The per-row score that Eq. 11 penalises by distance: the entropy H_j
+    of the row's softmax (Method: "distance-penalized entropy"), or, for
+    the confidence reading (Key claims §5.2: "distance-penalized confidence
+    rule"), the negative log of the row's top probability, -ln p_max.
+    Lower is more certain in both readings."""
+    if mode == SCORE_ENTROPY:
+        return np.asarray(scores.entropy, np.float64)
+    if mode == SCORE_NEGLOGP:
+        return -np.log(np.asarray(scores.p_max, np.float64))
+    raise ValueError(f"unknown score mode {mode}")
 
 
 def select_eq11(entropy, pos, observed, alpha, tau):
@@ -403,13 +469,16 @@ class SeqStep:
     k_win: list = field(default_factory=list)   # per layer [W][nkv][hd]
     v_win: list = field(default_factory=list)
     attn_out: list = field(default_factory=list)
+    x_mid: list = field(default_factory=list)   # per layer: residual after attention
 
 
 def forward_window(shape, weights, tokens_phys, pos_phys, pools, page_row,
-                   seq_len, store, visible=None, layers=None):
+                   seq_len, store, visible=None, layers=None, mid=None):
     """Causal forward of the reordered window on top of the cached prefix.
 
-    Returns (x_final, k_win per layer, v_win per layer, attn_out per layer).
+    Returns (x_final, k_win per layer, v_win per layer, attn_out per layer);
+    `mid` (a list, optional) receives each layer's residual stream between
+    its attention block and its FFN.
     """
     s = shape
     x = store(_f64(weights["embed"])[np.asarray(tokens_phys)])
@@ -418,7 +487,7 @@ def forward_window(shape, weights, tokens_phys, pos_phys, pools, page_row,
     for l in (range(s.n_layers) if layers is None else layers):
         kp, vp = pool_gather(pools[l], page_row, seq_len, s)
         x, k, v, o = layer_forward(s, weights["layers"][l], x, cos, sin,
-                                   kp, vp, store, visible)
+                                   kp, vp, store, visible, mid)
         ks.append(k)
         vs.append(v)
         os_.append(o)
@@ -427,24 +496,26 @@ def forward_window(shape, weights, tokens_phys, pos_phys, pools, page_row,
 
 def oracle_step_seq(shape, weights, tokens, pos, observed, seq_len, page_row,
                     pools, alpha, tau, plant_tok=None, plant_bias=0.0,
-                    write_pools=True):
+                    write_pools=True, score_mode=SCORE_ENTROPY):
     """One window decode step of one sequence.  `pools` (list of flat
     per-layer arrays) are updated in place with the committed K/V when
-    `write_pools` is set."""
+    `write_pools` is set.  `score_mode` picks the score Eq. 11 penalises
+    (slot_score)."""
     s = shape
     store = storer(s.dtype)
     tokens = np.asarray(tokens, np.int32)
     pos = np.asarray(pos, np.int32)
     obs = np.asarray(observed).astype(np.uint8)
     perm, inv = topological_reorder(obs)
+    mids = []
     x, ks, vs, os_ = forward_window(s, weights, tokens[perm], pos[perm],
-                                    pools, page_row, int(seq_len), store)
+                                    pools, page_row, int(seq_len), store, mid=mids)
     h = store(rmsnorm(x, weights["final_norm"], s.rms_eps))
     pt = None if plant_tok is None else np.asarray(plant_tok)[perm]
     sc = softmax_scores(lm_head_logits(h, weights["lm_head"], s.mask_id,
                                        pt, plant_bias))
     W = tokens.size
-    slot_H = np.where(obs.astype(bool), np.nan, sc.entropy[inv])
+    slot_H = np.where(obs.astype(bool), np.nan, slot_score(sc, score_mode)[inv])
     slot_a = sc.argmax[inv]
     fill, ht = select_eq11(slot_H, pos, obs, alpha, tau)
     c = commit_run(obs, pos, seq_len)
@@ -458,11 +529,11 @@ def oracle_step_seq(shape, weights, tokens, pos, observed, seq_len, page_row,
                    slot_argmax=slot_a, ht=ht, fill=fill, n_commit=c,
                    committed=tokens[:c].copy(), new_tokens=nt, new_pos=npos,
                    new_obs=nobs, new_seq_len=int(seq_len) + c, x_final=x,
-                   h_final=h, k_win=ks, v_win=vs, attn_out=os_)
+                   h_final=h, k_win=ks, v_win=vs, attn_out=os_, x_mid=mids)
 
 
 def oracle_step(shape, weights, state, pools, alpha, tau, plant_tok=None,
-                plant_bias=0.0, write_pools=True):
+                plant_bias=0.0, write_pools=True, score_mode=SCORE_ENTROPY):
     """One window decode step of a batch; per-sequence results."""
     out = []
     for b in range(state["tokens"].shape[0]):
@@ -471,7 +542,7 @@ def oracle_step(shape, weights, state, pools, alpha, tau, plant_tok=None,
             state["obs"][b], int(state["seq_len"][b]),
             state["page_table"][b], pools, alpha, tau,
             None if plant_tok is None else plant_tok[b], plant_bias,
-            write_pools))
+            write_pools, score_mode))
     return out
 
 

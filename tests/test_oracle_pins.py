@@ -529,3 +529,116 @@ def test_layer_forward_matches_torch_formulation():
     np.testing.assert_allclose(ours, xt.numpy(), atol=1e-11, rtol=0)
     np.testing.assert_allclose(k_o, k.numpy(), atol=1e-11, rtol=0)
     np.testing.assert_allclose(v_o, v.numpy(), atol=1e-11, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# the confidence reading of Eq. 11: score = -ln p_max
+# ---------------------------------------------------------------------------
+def test_negative_log_confidence_closed_forms():
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((6, 300)) * 3.0
+    sc = O.softmax_scores(z)
+    got = O.slot_score(sc, O.SCORE_NEGLOGP)
+    # -ln p_max = logsumexp(z) - max z (scipy's logsumexp, not the oracle's lse)
+    want = scipy.special.logsumexp(z, axis=1) - z.max(axis=1)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    assert np.all(got >= 0)
+    # uniform logits over V tokens: p_max = 1/V, score ln V (= the entropy)
+    V = 1000
+    u = O.softmax_scores(np.zeros((1, V)))
+    assert abs(O.slot_score(u, O.SCORE_NEGLOGP)[0] - math.log(V)) < 1e-12
+    assert abs(O.slot_score(u, O.SCORE_ENTROPY)[0] - math.log(V)) < 1e-12
+    # planted peak with p_top = 0.95 over equal other logits: score ln(1/0.95)
+    Vp = 151936
+    zp = np.zeros((1, Vp))
+    zp[0, 7] = plant_bias_for(Vp)
+    p = O.softmax_scores(zp)
+    assert abs(O.slot_score(p, O.SCORE_NEGLOGP)[0] - math.log(1 / 0.95)) < 1e-9
+    # the entropy reading is the default and equals the entropy field
+    np.testing.assert_array_equal(O.slot_score(sc, O.SCORE_ENTROPY), sc.entropy)
+    with pytest.raises(ValueError):
+        O.slot_score(sc, 7)
+
+
+def test_score_mode_changes_only_the_selection_score():
+    """A whole oracle step in the confidence reading: the forward, the
+    commit and the scores are those of the entropy reading; the fills are
+    Eq. 11 applied to -ln p_max (the definition, re-evaluated here through
+    the brute-force sort of all masked slots)."""
+    s = TINY
+    wl = Workload("t", s, batch=2, window=8, prefix=(40, 70), masked=(3, 6), seed=5)
+    st = make_state_np(wl)
+    w = make_weights_np(s, seed=5)
+    pools = [make_pool_np(s, st["num_pages"], 5, 0).astype(np.float64)]
+    ent = O.oracle_step(s, w, st, [p.copy() for p in pools], 0.05, 5.0)
+    neg = O.oracle_step(s, w, st, [p.copy() for p in pools], 0.05, 5.0,
+                        score_mode=O.SCORE_NEGLOGP)
+    for a, b, bb in zip(ent, neg, range(2)):
+        assert a.n_commit == b.n_commit and np.array_equal(a.scores.lse, b.scores.lse)
+        obs = st["obs"][bb].astype(bool)
+        pos = st["pos"][bb]
+        score = -np.log(b.scores.p_max[b.inv])
+        masked = [j for j in range(8) if not obs[j]]
+        m0 = masked[0]
+        ht = {j: np.float32(np.float32(score[j]) + np.float32(np.float32(0.05) *
+                                                            np.float32(pos[j] - pos[m0])))
+              for j in masked}
+        ordered = sorted(masked, key=lambda j: (float(ht[j]), j))
+        below = [j for j in ordered if ht[j] < np.float32(5.0)]
+        want = sorted(below) if below else [ordered[0]]
+        assert b.fill == want
+
+
+# ---------------------------------------------------------------------------
+# Dual-Stream Masking (Key claims §4.2, Eq. 8-10; Method)
+# ---------------------------------------------------------------------------
+def test_dual_stream_memory_rows_are_causal_self_attention():
+    """The memory stream is plain causal self-attention: torch's
+    scaled_dot_product_attention with is_causal over the memory tokens."""
+    rng = np.random.default_rng(21)
+    n, nq, nkv, hd, block = 48, 4, 2, 16, 16
+    q = rng.standard_normal((2 * n, nq, hd))
+    km, vm, kp, vp = (rng.standard_normal((n, nkv, hd)) for _ in range(4))
+    out = O.dual_stream_attention(q, km, vm, kp, vp, block)
+    qt = torch.from_numpy(q[:n]).permute(1, 0, 2)
+    kt = torch.from_numpy(np.repeat(km, nq // nkv, axis=1)).permute(1, 0, 2)
+    vt = torch.from_numpy(np.repeat(vm, nq // nkv, axis=1)).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True)
+    np.testing.assert_allclose(out[:n], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_dual_stream_prediction_block_is_an_inference_window_step():
+    """A prediction block attends exactly as the inference-time window step
+    does with the memory before the block as its cached prefix (the point of
+    Dual-Stream Masking: training sees the prefix-conditioned setting of
+    inference): window_attention(q_block, memory K/V of positions < j*block,
+    the block's own K/V) with the causal mask in the block's order.  The
+    first block sees no memory at all; blocks never see each other."""
+    rng = np.random.default_rng(22)
+    n, nq, nkv, hd, block = 64, 4, 2, 16, 16
+    q = rng.standard_normal((2 * n, nq, hd))
+    km, vm, kp, vp = (rng.standard_normal((n, nkv, hd)) for _ in range(4))
+    out = O.dual_stream_attention(q, km, vm, kp, vp, block)
+    for j in range(n // block):
+        rows = slice(j * block, (j + 1) * block)
+        ref = O.window_attention(q[n:][rows], km[:j * block], vm[:j * block], kp[rows], vp[rows])
+        np.testing.assert_allclose(out[n:][rows], ref, rtol=0, atol=1e-12)
+    # perturbing another block's prediction K/V changes nothing in block 1
+    kp2 = kp.copy()
+    kp2[2 * block:] += 5.0
+    out2 = O.dual_stream_attention(q, km, vm, kp2, vp, block)
+    np.testing.assert_array_equal(out2[n + block:n + 2 * block], out[n + block:n + 2 * block])
+    # and memory rows never see the prediction stream
+    np.testing.assert_array_equal(out2[:n], out[:n])
+
+
+def test_dual_stream_visibility_counts():
+    """Closed form: memory rows see r+1 keys; prediction row i of block j at
+    physical index p sees j*block + p + 1 keys."""
+    n, block = 48, 16
+    vis = O.dual_stream_visibility(n, block)
+    assert vis.sum(1)[:n].tolist() == [r + 1 for r in range(n)]
+    assert vis.sum(1)[n:].tolist() == [(i // block) * block + i % block + 1 for i in range(n)]
+    # no prediction row sees a memory token at or after its block's start
+    for i in range(n):
+        assert not vis[n + i, (i // block) * block:n].any()
