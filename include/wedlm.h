@@ -40,7 +40,9 @@
  * (zeros, say): the attention multiplies them by zero probabilities.
  *
  * Supported shapes: head_dim 64 or 128 (fp32) / 128 (bf16); window <= 64;
- * (n_q_heads / n_kv_heads) * window <= 128; max_batch * window <= 512.
+ * max_batch * window <= 512; bf16: G * window <= 128 or G divides 128
+ * (G = n_q_heads / n_kv_heads; the G * W query rows of a kv head run in
+ * blocks of 128 on the tensor cores); fp32: G * window <= 512.
  */
 #ifndef WEDLM_H
 #define WEDLM_H
@@ -73,6 +75,12 @@ enum {
 };
 
 enum { WEDLM_BF16 = 0, WEDLM_FP32 = 1 };
+
+/* Score of a masked slot in Eq. 11 (H~_j = score_j + alpha * d_j):
+ * the entropy of its softmax (the Method section's formula), or the
+ * confidence reading of the rule (Key claims §5.2, "distance-penalized
+ * confidence rule"): -ln p_max. */
+enum { WEDLM_SCORE_ENTROPY = 0, WEDLM_SCORE_NEGLOGP = 1 };
 
 typedef struct wedlm_ctx wedlm_ctx;
 
@@ -131,6 +139,7 @@ typedef struct wedlm_step_in {
   const int32_t *plant_token;  /* [B][W] token to bias per slot (-1: none), or NULL */
   float plant_bias;            /* added to that token's logit              */
   float alpha, tau;            /* Eq. 11 distance weight and threshold     */
+  int32_t score_mode;          /* WEDLM_SCORE_ENTROPY | WEDLM_SCORE_NEGLOGP */
 } wedlm_step_in;
 
 /* Outputs of one step (device pointers; optional ones may be NULL). */
@@ -190,6 +199,83 @@ int wedlm_launches_per_step(wedlm_ctx *ctx, int32_t batch);
 /* ---- the whole step (rows a1..a7) ------------------------------------- */
 int wedlm_step(wedlm_ctx *ctx, const wedlm_step_in *in, wedlm_step_out *out,
                void *stream);
+
+/* ---- prompt prefill and the streaming loop ------------------------------ */
+
+/* Prompt prefill (bud-325 summary page, Method: the decoder runs "on top of
+ * the persistent KV cache"): a causal forward of `chunk` prompt tokens per
+ * sequence, at logical positions seq_len[b] .. seq_len[b]+chunk-1, on top of
+ * each sequence's cached prefix; the K/V of every token of every layer are
+ * written to the pages, and seq_len[b] += chunk.  This is the window step
+ * with every slot observed and no selection.  tokens: [B][chunk] device;
+ * hidden: [B*chunk][hidden] final residual stream, or NULL.  Limits: B *
+ * chunk <= max_batch * window (the workspace rows) and B * (chunk rounded
+ * up to 16) <= max_batch * (window rounded up to 16); the attention limit on
+ * G * chunk as above.  Returns WEDLM_ERR_INVALID_ARG beyond them. */
+int wedlm_prefill(wedlm_ctx *ctx, int32_t batch, int32_t chunk, const int32_t *tokens,
+                  int32_t *seq_len, const int32_t *page_table, int32_t num_pages,
+                  void *const *kv_pools, void *hidden, void *stream);
+
+/* The streaming decode loop on the device (Key claims §5.2 and Method:
+ * reorder, forward, commit, select, refill, step after step, with a fixed
+ * window).  One call enqueues a CUDA graph whose conditional while-node
+ * runs the whole step (as wedlm_step) until `max_steps` steps have run or
+ * every sequence has stopped; no host round trip between steps.  The window
+ * arrays are updated in place.  Per sequence: a stopped sequence (done[b]
+ * = 1) is left unchanged; a sequence stops once its seq_len reaches
+ * stop_len[b] or after committing `stop_token`.  Committed tokens are
+ * written to out_tokens[b][p - out_base[b]] for logical position p when
+ * that index is in [0, out_cap).  All pointers are device pointers except
+ * kv_pools (host array of n_layers device pools). */
+typedef struct wedlm_gen_in {
+  int32_t batch;               /* B, 1..max_batch                          */
+  int32_t num_pages;           /* pages in each layer's pool               */
+  int32_t *tokens;             /* [B][W] window, updated in place          */
+  int32_t *pos;                /* [B][W]                                   */
+  uint8_t *observed;           /* [B][W]                                   */
+  int32_t *seq_len;            /* [B] committed length, advanced in place  */
+  const int32_t *page_table;   /* [B][max_pages_per_seq]                   */
+  void *const *kv_pools;       /* HOST array of n_layers device pools      */
+  const int32_t *plant_token;  /* [B][W] or NULL (as in wedlm_step_in)     */
+  float plant_bias;
+  float alpha, tau;            /* Eq. 11 distance weight and threshold     */
+  int32_t score_mode;          /* WEDLM_SCORE_*                            */
+  int32_t max_steps;           /* the loop runs at most this many steps    */
+  int32_t *done;               /* [B] stop flags, read and updated         */
+  const int32_t *stop_len;     /* [B] length budget, or NULL               */
+  int32_t stop_token;          /* token id that stops a sequence, -1: none */
+  int32_t *out_tokens;         /* [B][out_cap] committed ids, or NULL      */
+  const int32_t *out_base;     /* [B] position of out_tokens[b][0]         */
+  int32_t out_cap;
+  int32_t *steps_run;          /* [1] steps the loop ran, or NULL          */
+} wedlm_gen_in;
+int wedlm_generate(wedlm_ctx *ctx, const wedlm_gen_in *in, void *stream);
+
+/* ---- Dual-Stream Masking attention (training-time mask) ------------------ */
+
+/* Attention under Dual-Stream Masking (bud-325 summary page, Key claims
+ * §4.2, Eq. 8-10; Method): a clean memory stream of n tokens at logical
+ * positions 0..n-1 and a prediction stream over the same n positions, cut
+ * into blocks of `block` tokens, each block topologically reordered
+ * (observed tokens first) with its tokens keeping their logical positions.
+ * A memory row attends causally to the memory stream; a prediction row of
+ * block j attends to the memory tokens at positions before the block
+ * (0..j*block-1) and, causally in the block's physical order, to its own
+ * block.  Each block of either stream runs as one sequence of the paged
+ * window attention with prefix = the memory positions before the block.
+ *  q:        [2][n][n_q_heads][head_dim] bf16: memory rows, then prediction
+ *            rows (physical order inside each block); RoPE applied;
+ *  mem_pool: the memory stream's K/V as n/16 pages in order (page p holds
+ *            positions 16p..16p+15; the paged layout above, K after RoPE);
+ *  win:      [2][n/block][2 (K, V)][n_kv_heads][block][head_dim] bf16 in the
+ *            page tile layout: every block's own K/V, memory blocks first;
+ *  o:        [2][n][n_q_heads*head_dim] bf16.
+ * block a multiple of 16 dividing n; bf16 contexts only.  The partials use
+ * the context's attention workspace: shapes it cannot hold (2n/block
+ * blocks x n_kv_heads x row blocks units) return WEDLM_ERR_CAPACITY. */
+int wedlm_dual_stream_attention(wedlm_ctx *ctx, int32_t n, int32_t block, const void *q,
+                                const void *mem_pool, const void *win, void *o,
+                                void *stream);
 
 /* ---- one row of the step each (tests and composition) ------------------ */
 
@@ -251,7 +337,12 @@ int wedlm_lm_head(wedlm_ctx *ctx, int32_t batch, const void *x,
  *    WEDLM_ERR_INVALID_ARG.
  *  - Every call shares the array and it keeps the last call's contents:
  *    calls that overlap on the GPU (other streams, other threads) race.
- *  - Page ids outside [0, num_pages) read as zeros and are not reported.
+ *  - Nothing found on the device is reported: page ids outside
+ *    [0, num_pages) read as zeros, and a bounded wait that expires (2 s)
+ *    leaves the output partly written; the error word that records either
+ *    lives in the array and no call reads it back.
+ *  - q, kv_pool, kv_win and o must be 16-byte aligned; n_q_heads a positive
+ *    multiple of n_kv_heads.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine. */
 int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q_heads,
                            int32_t n_kv_heads, int32_t max_pages_per_seq,

@@ -19,13 +19,15 @@ OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CUDA, ERR_NUMERIC, ERR_TIMEOUT, ERR_DEVIC
 DEV_BAD_PAGE, DEV_CAPACITY, DEV_BAD_TOKEN, DEV_NUMERIC, DEV_TIMEOUT, DEV_BAD_SEQLEN = (
     1, 2, 4, 8, 16, 32)
 BF16, FP32 = 0, 1
+SCORE_ENTROPY, SCORE_NEGLOGP = 0, 1
 KINDS = ["reorder", "rmsnorm", "gemm_qkv", "attn", "attn_merge", "gemm_o",
          "gemm_gateup", "gemm_down", "lmhead", "lmhead_merge", "select", "commit"]
 
 EXPORTED = ["wedlm_create", "wedlm_destroy", "wedlm_last_error", "wedlm_get_status",
             "wedlm_set_graphs", "wedlm_set_timing", "wedlm_get_timings",
             "wedlm_launches_per_step", "wedlm_step", "wedlm_reorder_embed",
-            "wedlm_layer", "wedlm_attention", "wedlm_lm_head", "wedlm_attention_static"]
+            "wedlm_layer", "wedlm_attention", "wedlm_lm_head", "wedlm_attention_static",
+            "wedlm_prefill", "wedlm_generate", "wedlm_dual_stream_attention"]
 
 
 class Config(ctypes.Structure):
@@ -54,7 +56,18 @@ class StepIn(ctypes.Structure):
                 ("pos", c_void_p), ("observed", c_void_p), ("seq_len", c_void_p),
                 ("page_table", c_void_p), ("kv_pools", POINTER(c_void_p)),
                 ("plant_token", c_void_p), ("plant_bias", c_float), ("alpha", c_float),
-                ("tau", c_float)]
+                ("tau", c_float), ("score_mode", c_int32)]
+
+
+class GenIn(ctypes.Structure):
+    _fields_ = [("batch", c_int32), ("num_pages", c_int32), ("tokens", c_void_p),
+                ("pos", c_void_p), ("observed", c_void_p), ("seq_len", c_void_p),
+                ("page_table", c_void_p), ("kv_pools", POINTER(c_void_p)),
+                ("plant_token", c_void_p), ("plant_bias", c_float), ("alpha", c_float),
+                ("tau", c_float), ("score_mode", c_int32), ("max_steps", c_int32),
+                ("done", c_void_p), ("stop_len", c_void_p), ("stop_token", c_int32),
+                ("out_tokens", c_void_p), ("out_base", c_void_p), ("out_cap", c_int32),
+                ("steps_run", c_void_p)]
 
 
 class StepOut(ctypes.Structure):
@@ -88,6 +101,10 @@ def load_library(path: str = LIB_PATH):
     lib.wedlm_lm_head.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_float,
                                   c_void_p, c_void_p, c_void_p]
     lib.wedlm_attention_static.argtypes = [c_int32] * 6 + [c_void_p] * 7
+    lib.wedlm_prefill.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                  c_int32, POINTER(c_void_p), c_void_p, c_void_p]
+    lib.wedlm_generate.argtypes = [c_void_p, POINTER(GenIn), c_void_p]
+    lib.wedlm_dual_stream_attention.argtypes = [c_void_p, c_int32, c_int32] + [c_void_p] * 5
     return lib
 
 
@@ -232,7 +249,8 @@ class WedlmContext:
         return out
 
     def step(self, tokens, pos, observed, seq_len, page_table, pools, num_pages,
-             alpha, tau, out, plant_token=None, plant_bias=0.0, stream=None):
+             alpha, tau, out, plant_token=None, plant_bias=0.0, stream=None,
+             score_mode=SCORE_ENTROPY):
         """Enqueue one window decode step.  All tensors are CUDA tensors:
         tokens/pos int32 [B][W], observed uint8 [B][W], seq_len int32 [B]
         (updated in place), page_table int32 [B][max_pages_per_seq], pools a
@@ -244,12 +262,45 @@ class WedlmContext:
                      seq_len=seq_len.data_ptr(), page_table=page_table.data_ptr(),
                      kv_pools=ctypes.cast(pool_arr, POINTER(c_void_p)),
                      plant_token=None if plant_token is None else plant_token.data_ptr(),
-                     plant_bias=plant_bias, alpha=alpha, tau=tau)
+                     plant_bias=plant_bias, alpha=alpha, tau=tau, score_mode=score_mode)
         sout = StepOut(**{k: (out[k].data_ptr() if k in out else None)
                           for k, _ in StepOut._fields_})
         self._check(self._lib.wedlm_step(self._h, ctypes.byref(sin), ctypes.byref(sout),
                                          _stream_handle(stream)))
         return out
+
+    def prefill(self, tokens, seq_len, page_table, pools, num_pages, hidden=None, stream=None):
+        """Enqueue a prompt prefill: tokens int32 [B][chunk] at positions
+        seq_len[b].. (seq_len advanced in place); K/V of every layer to the
+        pages.  hidden: optional [B*chunk][hidden] output."""
+        B, C = tokens.shape
+        pool_arr = (c_void_p * len(pools))(*[p.data_ptr() for p in pools])
+        self._check(self._lib.wedlm_prefill(
+            self._h, B, C, _ptr(tokens), _ptr(seq_len), _ptr(page_table), num_pages,
+            ctypes.cast(pool_arr, POINTER(c_void_p)), _ptr(hidden), _stream_handle(stream)))
+
+    def generate(self, tokens, pos, observed, seq_len, page_table, pools, num_pages, alpha,
+                 tau, max_steps, done, stop_len=None, stop_token=-1, out_tokens=None,
+                 out_base=None, plant_token=None, plant_bias=0.0, score_mode=SCORE_ENTROPY,
+                 steps_run=None, stream=None):
+        """Enqueue the streaming loop on the device (up to max_steps steps,
+        window tensors updated in place; see wedlm_generate)."""
+        B = tokens.shape[0]
+        pool_arr = (c_void_p * len(pools))(*[p.data_ptr() for p in pools])
+        gin = GenIn(batch=B, num_pages=num_pages, tokens=tokens.data_ptr(), pos=pos.data_ptr(),
+                    observed=observed.data_ptr(), seq_len=seq_len.data_ptr(),
+                    page_table=page_table.data_ptr(),
+                    kv_pools=ctypes.cast(pool_arr, POINTER(c_void_p)),
+                    plant_token=None if plant_token is None else plant_token.data_ptr(),
+                    plant_bias=plant_bias, alpha=alpha, tau=tau, score_mode=score_mode,
+                    max_steps=max_steps, done=done.data_ptr(),
+                    stop_len=None if stop_len is None else stop_len.data_ptr(),
+                    stop_token=stop_token,
+                    out_tokens=None if out_tokens is None else out_tokens.data_ptr(),
+                    out_base=None if out_base is None else out_base.data_ptr(),
+                    out_cap=0 if out_tokens is None else out_tokens.shape[1],
+                    steps_run=None if steps_run is None else steps_run.data_ptr())
+        self._check(self._lib.wedlm_generate(self._h, ctypes.byref(gin), _stream_handle(stream)))
 
     # -- single rows of the step --------------------------------------------
     def reorder_embed(self, tokens, pos, observed, perm, inv, x_out, pos_phys, stream=None):
@@ -269,6 +320,12 @@ class WedlmContext:
         self._check(self._lib.wedlm_attention(
             self._h, seq_len.shape[0], _ptr(q), _ptr(pool), _ptr(page_table),
             _ptr(seq_len), num_pages, _ptr(kv_win), _ptr(o), _stream_handle(stream)))
+
+    def dual_stream_attention(self, n, block, q, mem_pool, win, o, stream=None):
+        """Dual-Stream Masking attention (see wedlm_dual_stream_attention)."""
+        self._check(self._lib.wedlm_dual_stream_attention(
+            self._h, n, block, _ptr(q), _ptr(mem_pool), _ptr(win), _ptr(o),
+            _stream_handle(stream)))
 
     def lm_head(self, batch, x, rows_out, plant_token=None, plant_bias=0.0, logits=None,
                 stream=None):

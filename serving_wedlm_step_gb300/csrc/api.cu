@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <memory>
 #include <string>
+#include <type_traits>
 #include <vector>
 
 #include "gemm_tc.h"
@@ -24,6 +25,8 @@ struct GraphEntry {
 
 constexpr int kMaxGraphs = 4;
 constexpr int kMaxEvents = 8192;
+constexpr int kDualMaxBlocks = 512;   // blocks of both streams (sequences of one launch)
+constexpr int kDualMaxPages = 4096;   // memory stream of up to 65536 tokens
 
 }  // namespace
 
@@ -50,7 +53,12 @@ struct wedlm_ctx {
   size_t win_layer_stride = 0;  // elements
   float *attn_o = nullptr, *attn_ml = nullptr;
   int attn_chunk = 0, attn_max_chunks = 0;
-  int* attn_unit_cnt = nullptr;   // tensor-core attention: [B*nkv] segment counts
+  int* attn_unit_cnt = nullptr;   // tensor-core attention: segment counts per unit
+  size_t attn_units_cap = 0;      // units the counters and partials are sized for
+  int* gen_ctrl = nullptr;        // streaming loop: [0] steps left, [1] steps run
+  int32_t *gen_committed = nullptr, *gen_ncommitted = nullptr;  // its per-step outputs
+  size_t attn_part_rows = 0;      // rows of partial O the attention may use
+  int32_t *dual_len = nullptr, *dual_pt = nullptr;  // dual-stream block lengths, page row
   float* gemm_part = nullptr;
   size_t gemm_part_elems = 0;
   int* gemm_counters = nullptr;
@@ -66,6 +74,7 @@ struct wedlm_ctx {
   std::string last_error = "ok";
   bool use_graphs = true;
   std::vector<GraphEntry> graphs;
+  std::vector<GraphEntry> gen_graphs;  // streaming loops (conditional while node)
   uint64_t graph_clock = 0;
   // timing
   bool timing = false;
@@ -182,14 +191,31 @@ cudaError_t run_attention<bf16>(wedlm_ctx* c, const AttnArgs& A, cudaStream_t st
   return launch_attention_tc(A, c->zero_page, c->num_sms, st);
 }
 
-AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
+// Rows of one sequence in a call: the decode window (W slots) or a prefill
+// chunk; Wp = W rounded up to a page.
+struct Win {
+  int W, Wp;
+};
+Win ctx_win(const wedlm_ctx* c) { return Win{c->cfg.window, c->Wp}; }
+Win chunk_win(int chunk) { return Win{chunk, (chunk + kPageBlock - 1) / kPageBlock * kPageBlock}; }
+
+// Commit of the window rows of a call into the paged cache (QKV epilogue):
+// per sequence, rows 0..n[b]-1 go to positions base[b]..; n == null: none.
+struct Commit {
+  const int32_t* n = nullptr;
+  const int32_t* base = nullptr;
+  const int32_t* page_table = nullptr;
+  int num_pages = 0;
+};
+
+AttnArgs attn_args(wedlm_ctx* c, int B, Win win, const void* q, const void* pool,
                    const int32_t* page_table, const int32_t* seq_len,
                    int num_pages, const void* kv_win, void* o) {
   const wedlm_config& g = c->cfg;
   AttnArgs A{};
-  A.B = B; A.W = g.window; A.Wp = c->Wp; A.nq = g.n_q_heads; A.nkv = g.n_kv_heads;
+  A.B = B; A.W = win.W; A.Wp = win.Wp; A.nq = g.n_q_heads; A.nkv = g.n_kv_heads;
   A.hd = g.head_dim; A.chunk = c->attn_chunk; A.max_chunks = c->attn_max_chunks;
-  A.num_pages = num_pages; A.max_pages = g.max_pages_per_seq;
+  A.num_pages = num_pages; A.max_pages = g.max_pages_per_seq; A.pt_stride = g.max_pages_per_seq;
   A.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.head_dim));
   A.q = q; A.pool = pool; A.page_table = page_table; A.seq_len = seq_len;
   A.kv_win = kv_win; A.part_o = c->attn_o; A.part_ml = c->attn_ml; A.o = o;
@@ -200,7 +226,8 @@ AttnArgs attn_args(wedlm_ctx* c, int B, const void* q, const void* pool,
 }
 
 // The four projections of layer l on workspace activations (M rows).
-GemmProblem qkv_problem(wedlm_ctx* c, int l, int M, void* kv_win_layer) {
+GemmProblem qkv_problem(wedlm_ctx* c, int l, int M, Win win, void* kv_win_layer,
+                        const Commit& cm, void* pool) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
   const int nq = g.n_q_heads, nkv = g.n_kv_heads, hd = g.head_dim;
@@ -211,8 +238,11 @@ GemmProblem qkv_problem(wedlm_ctx* c, int l, int M, void* kv_win_layer) {
   GemmEpi& e = P.epi;
   e.mode = EPI_QKV; e.q_out = c->q; e.kv_win = kv_win_layer;
   e.cosb = c->cosb; e.sinb = c->sinb; e.q_norm = w.q_norm; e.k_norm = w.k_norm;
-  e.qk_norm = g.qk_norm; e.W = g.window; e.Wp = c->Wp; e.nq = nq; e.nkv = nkv;
+  e.qk_norm = g.qk_norm; e.W = win.W; e.Wp = win.Wp; e.nq = nq; e.nkv = nkv;
   e.hd = hd; e.eps = g.rms_eps;
+  e.commit_n = cm.n; e.commit_base = cm.base; e.page_table = cm.page_table;
+  e.pool = pool; e.max_pages = g.max_pages_per_seq; e.num_pages = cm.num_pages;
+  e.err = c->err;
   return P;
 }
 GemmProblem o_problem(wedlm_ctx* c, int l, int M, void* x, bool fuse) {
@@ -266,16 +296,16 @@ GemmProblem lmhead_problem(wedlm_ctx* c, int M) {
 // next layer's attention norm or the final norm).  Both are used on the
 // tensor-core path only, where the residual epilogue can fuse the norm.
 template <typename T>
-int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
+int layer_impl(wedlm_ctx* c, int l, int B, Win win, T* x, const int32_t* seq_len,
                const int32_t* page_table, int num_pages, const void* pool,
                void* kv_win_layer, cudaStream_t st, bool xn_ready = false,
-               const void* next_norm = nullptr) {
+               const void* next_norm = nullptr, const Commit& cm = Commit()) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
-  const int M = B * g.window, H = g.hidden;
+  const int M = B * win.W, H = g.hidden;
   const bool fuse = g.dtype == WEDLM_BF16;
   int rc;
-  GemmProblem Pqkv = qkv_problem(c, l, M, kv_win_layer);
+  GemmProblem Pqkv = qkv_problem(c, l, M, win, kv_win_layer, cm, const_cast<void*>(pool));
   GemmProblem Po = o_problem(c, l, M, x, fuse);
   GemmProblem Pgu = gateup_problem(c, l, M);
   GemmProblem Pd = down_problem(c, l, M, x, fuse ? next_norm : nullptr);
@@ -283,15 +313,13 @@ int layer_impl(wedlm_ctx* c, int l, int B, T* x, const int32_t* seq_len,
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
   if ((rc = run_gemm<T>(c, Pqkv, WEDLM_KIND_GEMM_QKV, st))) return rc;
-  AttnArgs A = attn_args(c, B, c->q, pool, page_table, seq_len, num_pages,
+  AttnArgs A = attn_args(c, B, win, c->q, pool, page_table, seq_len, num_pages,
                          kv_win_layer, c->o);
-  if (g.dtype == WEDLM_BF16) {
-    // tensor-core attention: one kernel (the segment merge is inside)
-    LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
-  } else {
-    LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
-    LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<T>(A, st));
-  }
+  // bf16: tensor-core attention, one kernel (the segment merge is inside);
+  // fp32: CUDA-core split-KV attention and its merge kernel
+  LAUNCH(c, WEDLM_KIND_ATTN, st, run_attention<T>(c, A, st));
+  if constexpr (std::is_same<T, float>::value)
+    LAUNCH(c, WEDLM_KIND_ATTN_MERGE, st, launch_attention_merge<float>(A, st));
   if ((rc = run_gemm<T>(c, Po, WEDLM_KIND_GEMM_O, st))) return rc;
   if (!fuse)
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
@@ -343,23 +371,41 @@ int check_step_args(wedlm_ctx* c, const wedlm_step_in* in, const wedlm_step_out*
       (const void*)out->new_pos == (const void*)in->pos ||
       (const void*)out->new_observed == (const void*)in->observed)
     return fail(c, WEDLM_ERR_INVALID_ARG, "outputs alias inputs");
+  if (in->score_mode != WEDLM_SCORE_ENTROPY && in->score_mode != WEDLM_SCORE_NEGLOGP)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "unknown score_mode");
   return WEDLM_OK;
 }
 
+// Streaming-loop controls of a step (all optional; see SelArgs).
+struct StepExtras {
+  int score_mode = 0;
+  int32_t* done = nullptr;
+  const int32_t* stop_len = nullptr;
+  int stop_token = -1;
+  int32_t* out_tokens = nullptr;
+  const int32_t* out_base = nullptr;
+  int out_cap = 0;
+};
+
 template <typename T>
 int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
-                  cudaStream_t st) {
+                  cudaStream_t st, const StepExtras& x) {
   const wedlm_config& g = c->cfg;
   const int B = in->batch, W = g.window, M = B * W;
   int rc;
+  // reorder + embed; also snapshots seq_len and counts the commit run of
+  // every sequence, so the QKV epilogues write the committed K/V to pages
   LAUNCH(c, WEDLM_KIND_REORDER, st,
          launch_reorder_embed<T>(B, W, g.hidden, g.head_dim, g.vocab,
                                  g.max_pages_per_seq * kPageBlock, in->tokens,
                                  in->pos, in->observed, in->seq_len,
                                  in->plant_token, (const T*)c->embed, c->inv_freq,
-                                 c->perm, c->inv, c->pos_phys, c->seq_snap,
-                                 c->plant_phys, (T*)c->x, c->cosb, c->sinb,
+                                 c->perm, c->inv, c->pos_phys, c->seq_snap, c->ncommit,
+                                 x.done, c->plant_phys, (T*)c->x, c->cosb, c->sinb,
                                  c->err, st));
+  Commit cm;
+  cm.n = c->ncommit; cm.base = c->seq_snap; cm.page_table = in->page_table;
+  cm.num_pages = in->num_pages;
   // on the tensor-core path each down projection also normalises x for
   // the next layer (or the LM head)
   const bool fuse = g.dtype == WEDLM_BF16;
@@ -367,9 +413,9 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
     void* win = (char*)c->kv_win + (size_t)l * c->win_layer_stride * c->es;
     const void* next_norm =
         !fuse ? nullptr : (l + 1 < g.n_layers ? c->layers[l + 1].attn_norm : c->final_norm);
-    if ((rc = layer_impl<T>(c, l, B, (T*)c->x, c->seq_snap, in->page_table,
+    if ((rc = layer_impl<T>(c, l, B, ctx_win(c), (T*)c->x, c->seq_snap, in->page_table,
                             in->num_pages, in->kv_pools[l], win, st, fuse && l > 0,
-                            next_norm)))
+                            next_norm, cm)))
       return rc;
   }
   if ((rc = lmhead_impl<T>(c, B, (const T*)c->x,
@@ -378,20 +424,15 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
     return rc;
   SelArgs S{};
   S.B = B; S.W = W; S.mask_id = g.mask_id; S.alpha = in->alpha; S.tau = in->tau;
+  S.score_mode = x.score_mode; S.done = x.done; S.stop_len = x.stop_len;
+  S.stop_token = x.stop_token; S.out_tokens = x.out_tokens; S.out_base = x.out_base;
+  S.out_cap = x.out_cap;
   S.tokens = in->tokens; S.pos = in->pos; S.obs = in->observed;
   S.seq_snap = c->seq_snap; S.seq_len = in->seq_len; S.inv = c->inv; S.rows = c->rows;
   S.new_tokens = out->new_tokens; S.new_pos = out->new_pos;
   S.new_obs = out->new_observed; S.committed = out->committed;
   S.n_committed = out->n_committed; S.ncommit_ws = c->ncommit; S.filled = out->filled;
   LAUNCH(c, WEDLM_KIND_SELECT, st, launch_select(S, st));
-  CommitArgs C{};
-  C.B = B; C.W = W; C.Wp = c->Wp; C.nkv = g.n_kv_heads; C.hd = g.head_dim;
-  C.n_layers = g.n_layers; C.max_pages = g.max_pages_per_seq; C.num_pages = in->num_pages;
-  C.win_layer_stride = c->win_layer_stride; C.kv_win = c->kv_win; C.inv = c->inv;
-  C.seq_snap = c->seq_snap; C.ncommit = c->ncommit; C.page_table = in->page_table;
-  C.err = c->err;
-  for (int l = 0; l < g.n_layers; ++l) C.pools.p[l] = in->kv_pools[l];
-  LAUNCH(c, WEDLM_KIND_COMMIT, st, launch_commit<T>(C, st));
   if (out->perm)
     CUDA_TRY(c, cudaMemcpyAsync(out->perm, c->perm, (size_t)M * 4,
                                 cudaMemcpyDeviceToDevice, st));
@@ -405,10 +446,10 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
 }
 
 int dispatch_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
-                  cudaStream_t st) {
+                  cudaStream_t st, const StepExtras& x) {
   c->launch_count = 0;
-  const int rc = c->cfg.dtype == WEDLM_BF16 ? step_launches<bf16>(c, in, out, st)
-                                            : step_launches<float>(c, in, out, st);
+  const int rc = c->cfg.dtype == WEDLM_BF16 ? step_launches<bf16>(c, in, out, st, x)
+                                            : step_launches<float>(c, in, out, st, x);
   if (rc == WEDLM_OK) c->last_step_launches = c->launch_count;
   return rc;
 }
@@ -422,11 +463,166 @@ std::vector<uint64_t> graph_key(const wedlm_ctx* c, const wedlm_step_in* in,
   k.push_back((uint64_t)in->num_pages);
   P(in->tokens); P(in->pos); P(in->observed); P(in->seq_len); P(in->page_table);
   P(in->plant_token); F(in->plant_bias); F(in->alpha); F(in->tau);
+  k.push_back((uint64_t)(uint32_t)in->score_mode);
   for (int l = 0; l < c->cfg.n_layers; ++l) P(in->kv_pools[l]);
   P(out->new_tokens); P(out->new_pos); P(out->new_observed); P(out->committed);
   P(out->n_committed); P(out->perm); P(out->filled); P(out->rows); P(out->logits);
   P(out->hidden);
   return k;
+}
+
+// ---------------------------------------------------------------------------
+// the streaming loop on the device: a conditional while node whose body is
+// one step plus gen_next_kernel; the loop ends when the step budget is spent
+// or every sequence has stopped
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int any_active(int B, const int32_t* done) {
+  int any = 0;
+  for (int b = 0; b < B; ++b) any |= (done[b] == 0);
+  return any;
+}
+
+__global__ void gen_init_kernel(int B, int max_steps, const int32_t* done, int* ctrl,
+                                int32_t* steps_run, cudaGraphConditionalHandle h) {
+  if (threadIdx.x != 0) return;
+  ctrl[0] = max_steps;  // steps left
+  ctrl[1] = 0;          // steps run
+  if (steps_run) *steps_run = 0;
+  cudaGraphSetConditional(h, (max_steps > 0 && any_active(B, done)) ? 1u : 0u);
+}
+
+// after every step: one step fewer left; continue while steps are left and a
+// sequence is still active (so the loop runs at most max_steps times)
+__global__ void gen_next_kernel(int B, const int32_t* done, int* ctrl, int32_t* steps_run,
+                                cudaGraphConditionalHandle h) {
+  if (threadIdx.x != 0) return;
+  const int left = ctrl[0] - 1, ran = ctrl[1] + 1;
+  ctrl[0] = left;
+  ctrl[1] = ran;
+  if (steps_run) *steps_run = ran;
+  cudaGraphSetConditional(h, (left > 0 && any_active(B, done)) ? 1u : 0u);
+}
+
+// Dual-Stream Masking as paged window attention: sequence s < nb is memory
+// block s, sequence nb + j prediction block j; both have the memory
+// positions 0..j*block-1 as cached prefix (one identity page-table row).
+__global__ void dual_setup_kernel(int nb, int block, int n_pages, int32_t* len, int32_t* pt) {
+  const int n = max(2 * nb, n_pages);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    if (i < 2 * nb) len[i] = (i % nb) * block;
+    if (i < n_pages) pt[i] = i;
+  }
+}
+
+int check_gen_args(wedlm_ctx* c, const wedlm_gen_in* in) {
+  const wedlm_config& g = c->cfg;
+  if (!in) return fail(c, WEDLM_ERR_INVALID_ARG, "null generate input");
+  if (in->batch < 1 || in->batch > g.max_batch)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "batch outside 1..max_batch");
+  if (in->num_pages < 1 || in->max_steps < 0)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "num_pages < 1 or max_steps < 0");
+  if (!in->tokens || !in->pos || !in->observed || !in->seq_len || !in->page_table ||
+      !in->kv_pools || !in->done)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "null input pointer");
+  for (int l = 0; l < g.n_layers; ++l)
+    if (!in->kv_pools[l] || ((uintptr_t)in->kv_pools[l] & 15))
+      return fail(c, WEDLM_ERR_INVALID_ARG, "null or misaligned kv pool");
+  if (in->out_tokens && (!in->out_base || in->out_cap < 1))
+    return fail(c, WEDLM_ERR_INVALID_ARG, "out_tokens without out_base / out_cap");
+  if (in->score_mode != WEDLM_SCORE_ENTROPY && in->score_mode != WEDLM_SCORE_NEGLOGP)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "unknown score_mode");
+  return WEDLM_OK;
+}
+
+std::vector<uint64_t> gen_key(const wedlm_ctx* c, const wedlm_gen_in* in) {
+  std::vector<uint64_t> k;
+  auto P = [&](const void* p) { k.push_back((uint64_t)(uintptr_t)p); };
+  auto F = [&](float f) { uint32_t u; memcpy(&u, &f, 4); k.push_back(u); };
+  k.push_back((uint64_t)in->batch);
+  k.push_back((uint64_t)in->num_pages);
+  P(in->tokens); P(in->pos); P(in->observed); P(in->seq_len); P(in->page_table);
+  P(in->plant_token); F(in->plant_bias); F(in->alpha); F(in->tau);
+  k.push_back((uint64_t)(uint32_t)in->score_mode);
+  k.push_back((uint64_t)(uint32_t)in->max_steps);
+  P(in->done); P(in->stop_len); k.push_back((uint64_t)(uint32_t)in->stop_token);
+  P(in->out_tokens); P(in->out_base); k.push_back((uint64_t)(uint32_t)in->out_cap);
+  P(in->steps_run);
+  for (int l = 0; l < c->cfg.n_layers; ++l) P(in->kv_pools[l]);
+  return k;
+}
+
+// Build the loop graph: gen_init_kernel -> while (cond) { step; gen_next_kernel }.
+int build_gen_graph(wedlm_ctx* c, const wedlm_gen_in* in, cudaGraphExec_t* exec_out) {
+  const wedlm_config& g = c->cfg;
+  cudaGraph_t graph = nullptr;
+  CUDA_TRY(c, cudaGraphCreate(&graph, 0));
+  struct GraphGuard {
+    cudaGraph_t g;
+    ~GraphGuard() { if (g) cudaGraphDestroy(g); }
+  } guard{graph};
+  cudaGraphConditionalHandle h;
+  CUDA_TRY(c, cudaGraphConditionalHandleCreate(&h, graph, 0, 0));
+  // the init kernel, then the conditional node after it
+  cudaGraphNode_t init = nullptr;
+  {
+    cudaKernelNodeParams kp = {};
+    int B = in->batch, ms = in->max_steps;
+    const int32_t* done = in->done;
+    int* ctrl = c->gen_ctrl;
+    int32_t* sr = in->steps_run;
+    void* args[] = {&B, &ms, &done, &ctrl, &sr, &h};
+    kp.func = (void*)gen_init_kernel;
+    kp.gridDim = dim3(1);
+    kp.blockDim = dim3(32);
+    kp.kernelParams = args;
+    CUDA_TRY(c, cudaGraphAddKernelNode(&init, graph, nullptr, 0, &kp));
+  }
+  cudaGraphNodeParams cp = {};
+  cp.type = cudaGraphNodeTypeConditional;
+  cp.conditional.handle = h;
+  cp.conditional.type = cudaGraphCondTypeWhile;
+  cp.conditional.size = 1;
+  cudaGraphNode_t cnode = nullptr;
+  CUDA_TRY(c, cudaGraphAddNode(&cnode, graph, &init, nullptr, 1, &cp));
+  cudaGraph_t body = cp.conditional.phGraph_out[0];
+  // the body: one step with the window updated in place, then the control
+  wedlm_step_in sin{};
+  sin.batch = in->batch; sin.num_pages = in->num_pages; sin.tokens = in->tokens;
+  sin.pos = in->pos; sin.observed = in->observed; sin.seq_len = in->seq_len;
+  sin.page_table = in->page_table; sin.kv_pools = in->kv_pools;
+  sin.plant_token = in->plant_token; sin.plant_bias = in->plant_bias;
+  sin.alpha = in->alpha; sin.tau = in->tau; sin.score_mode = in->score_mode;
+  wedlm_step_out sout{};
+  sout.new_tokens = in->tokens; sout.new_pos = in->pos; sout.new_observed = in->observed;
+  sout.committed = c->gen_committed; sout.n_committed = c->gen_ncommitted;
+  StepExtras x;
+  x.score_mode = in->score_mode; x.done = in->done; x.stop_len = in->stop_len;
+  x.stop_token = in->stop_token; x.out_tokens = in->out_tokens; x.out_base = in->out_base;
+  x.out_cap = in->out_cap;
+  CUDA_TRY(c, cudaStreamBeginCaptureToGraph(c->cap_stream, body, nullptr, nullptr, 0,
+                                            cudaStreamCaptureModeThreadLocal));
+  // a loop body holds kernels only: no timing events inside it
+  const bool timing = c->timing;
+  c->timing = false;
+  int rc = dispatch_step(c, &sin, &sout, c->cap_stream, x);
+  c->timing = timing;
+  if (rc == WEDLM_OK) {
+    gen_next_kernel<<<1, 32, 0, c->cap_stream>>>(in->batch, in->done, c->gen_ctrl,
+                                                 in->steps_run, h);
+    c->launch_count += 1;
+  }
+  cudaGraph_t captured = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &captured);
+  if (rc) return rc;
+  if (ce != cudaSuccess)
+    return fail(c, WEDLM_ERR_CUDA, std::string("loop capture: ") + cudaGetErrorString(ce));
+  (void)g;
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+  if (ie != cudaSuccess)
+    return fail(c, WEDLM_ERR_CUDA, std::string("loop instantiate: ") + cudaGetErrorString(ie));
+  *exec_out = exec;
+  return WEDLM_OK;
 }
 
 }  // namespace
@@ -450,15 +646,19 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
       bad(g.mask_id < 0 || g.mask_id >= g.vocab) ||
       bad(g.window < 1 || g.window > kMaxWindow) || bad(g.page_block != kPageBlock) ||
       bad(g.max_batch < 1 || g.max_batch * g.window > kMaxRows) ||
-      bad((g.n_q_heads / g.n_kv_heads) * g.window > 128) ||
       bad(g.max_pages_per_seq < 1) ||
       bad(g.dtype != WEDLM_BF16 && g.dtype != WEDLM_FP32) ||
       bad(!(g.rope_theta > 0.f) || !(g.rms_eps >= 0.f)))
     return WEDLM_ERR_INVALID_ARG;
-  // bf16: tensor-core GEMMs (K multiple of 64) and attention (head_dim 128)
+  // bf16: tensor-core GEMMs (K multiple of 64) and attention (head_dim 128,
+  // query rows of a kv head in row blocks); fp32: CUDA-core attention with
+  // at most 512 query rows per kv head
   if (g.dtype == WEDLM_BF16 &&
       ((g.hidden % 64) || ((g.n_q_heads * g.head_dim) % 64) || (g.ffn % 64) ||
-       g.head_dim != 128))
+       g.head_dim != 128 ||
+       attention_tc_row_blocks(g.n_q_heads, g.n_kv_heads, g.window, nullptr) == 0))
+    return WEDLM_ERR_INVALID_ARG;
+  if (g.dtype == WEDLM_FP32 && (g.n_q_heads / g.n_kv_heads) * g.window > 512)
     return WEDLM_ERR_INVALID_ARG;
   if (!w->embed || !w->final_norm || !w->lm_head || !w->attn_norm || !w->w_q ||
       !w->w_k || !w->w_v || !w->w_o || !w->ffn_norm || !w->w_gate || !w->w_up ||
@@ -515,13 +715,25 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   WA(C->act, M * g.ffn * es);
   WA(C->kv_win, C->win_layer_stride * g.n_layers * es);
   // split-KV partials: per (sequence, kv head, chunk) for the CUDA-core
-  // attention; per segment (at most one per SM plus one per unit) for the
-  // tensor-core attention
+  // attention (rows * chunks, the same bound for a prefill chunk since
+  // B * chunk <= max_batch * window); per segment for the tensor-core
+  // attention: at most one per block (SM) plus one per unit (sequence x kv
+  // head x row block), of at most 128 rows, where the rows of all units'
+  // row blocks together stay below nkv * (G * M_max + 128 * max_batch)
   const size_t units = (size_t)g.max_batch * g.n_kv_heads;
-  const size_t slots = std::max(units * C->attn_max_chunks, (size_t)C->num_sms + units);
-  WA(C->attn_o, slots * R * hd * 4);
-  WA(C->attn_ml, slots * R * 2 * 4);
-  WA(C->attn_unit_cnt, units * 4);
+  const size_t G = (size_t)(g.n_q_heads / g.n_kv_heads);
+  const size_t simt_rows = units * C->attn_max_chunks * R;
+  const size_t tc_rows = (size_t)C->num_sms * 128 +
+                         (size_t)g.n_kv_heads * (G * M + 128 * (size_t)g.max_batch);
+  const size_t part_rows = g.dtype == WEDLM_BF16 ? tc_rows : simt_rows;
+  C->attn_units_cap = (size_t)g.n_kv_heads * M;  // B * nkv * row blocks <= nkv * B * chunk
+  WA(C->attn_o, part_rows * hd * 4);
+  WA(C->attn_ml, part_rows * 2 * 4);
+  WA(C->attn_unit_cnt, C->attn_units_cap * 4);
+  WA(C->gen_ctrl, 256);
+  C->attn_part_rows = part_rows;
+  WA(C->dual_len, (size_t)kDualMaxBlocks * 4); WA(C->dual_pt, (size_t)kDualMaxPages * 4);
+  WA(C->gen_committed, M * 4); WA(C->gen_ncommitted, g.max_batch * 4);
   WA(C->gemm_part, C->gemm_part_elems * 4);
   WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
   WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
@@ -565,6 +777,8 @@ void wedlm_destroy(wedlm_ctx* c) {
   cudaDeviceSynchronize();
   for (auto& g : c->graphs)
     if (g.exec) cudaGraphExecDestroy(g.exec);
+  for (auto& g : c->gen_graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
   for (auto e : c->ev) cudaEventDestroy(e);
   for (void* p : c->allocs) cudaFree(p);
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
@@ -582,9 +796,7 @@ int wedlm_get_status(wedlm_ctx* c, int32_t* device_error) {
   CUDA_TRY(c, cudaMemcpy(&word, c->err, 4, cudaMemcpyDeviceToHost));
   CUDA_TRY(c, cudaMemset(c->err, 0, 4));
   // a launch that gave up on a wait may have left segment counts behind
-  if (word)
-    CUDA_TRY(c, cudaMemset(c->attn_unit_cnt, 0,
-                           (size_t)c->cfg.max_batch * c->cfg.n_kv_heads * 4));
+  if (word) CUDA_TRY(c, cudaMemset(c->attn_unit_cnt, 0, c->attn_units_cap * 4));
   if (device_error) *device_error = word;
   if (word) return fail(c, WEDLM_ERR_DEVICE, "device error word " + std::to_string(word));
   return WEDLM_OK;
@@ -644,10 +856,12 @@ int wedlm_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out, void*
   if (rc) return rc;
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
+  StepExtras x;
+  x.score_mode = in->score_mode;
   if (c->timing || !c->use_graphs) {
     if (c->timing && c->ev_used + 4 * wedlm_launches_per_step(c, in->batch) > kMaxEvents)
       if ((rc = harvest_events(c))) return rc;
-    return dispatch_step(c, in, out, st);
+    return dispatch_step(c, in, out, st, x);
   }
   std::vector<uint64_t> key = graph_key(c, in, out);
   GraphEntry* hit = nullptr;
@@ -657,7 +871,7 @@ int wedlm_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out, void*
     // capture on the library's own stream, replay on the caller's
     cudaGraph_t graph = nullptr;
     CUDA_TRY(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
-    rc = dispatch_step(c, in, out, c->cap_stream);
+    rc = dispatch_step(c, in, out, c->cap_stream, x);
     cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &graph);
     if (rc) {
       if (graph) cudaGraphDestroy(graph);
@@ -686,6 +900,128 @@ int wedlm_step(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out, void*
   return WEDLM_OK;
 }
 
+int wedlm_prefill(wedlm_ctx* c, int32_t batch, int32_t chunk, const int32_t* tokens,
+                  int32_t* seq_len, const int32_t* page_table, int32_t num_pages,
+                  void* const* kv_pools, void* hidden, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  const Win win = chunk_win(chunk);
+  const int G = g.n_q_heads / g.n_kv_heads;
+  if (batch < 1 || batch > g.max_batch || chunk < 1 || batch * chunk > c->M_max ||
+      batch * win.Wp > g.max_batch * c->Wp || !tokens || !seq_len || !page_table ||
+      !kv_pools || num_pages < 1)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad prefill arguments");
+  if (g.dtype == WEDLM_BF16
+          ? attention_tc_row_blocks(g.n_q_heads, g.n_kv_heads, chunk, nullptr) == 0
+          : G * chunk > 512)
+    return fail(c, WEDLM_ERR_INVALID_ARG, "prefill chunk too large for the attention");
+  for (int l = 0; l < g.n_layers; ++l)
+    if (!kv_pools[l] || ((uintptr_t)kv_pools[l] & 15))
+      return fail(c, WEDLM_ERR_INVALID_ARG, "null or misaligned kv pool");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  c->launch_count = 0;
+  const int M = batch * chunk;
+  const int page_cap = g.max_pages_per_seq * kPageBlock;
+  if (g.dtype == WEDLM_BF16)
+    LAUNCH(c, WEDLM_KIND_REORDER, st,
+           launch_prefill_embed<bf16>(batch, chunk, g.hidden, g.head_dim, g.vocab, page_cap,
+                                      tokens, seq_len, (const bf16*)c->embed, c->inv_freq,
+                                      c->pos_phys, c->seq_snap, c->ncommit, (bf16*)c->x,
+                                      c->cosb, c->sinb, c->err, st));
+  else
+    LAUNCH(c, WEDLM_KIND_REORDER, st,
+           launch_prefill_embed<float>(batch, chunk, g.hidden, g.head_dim, g.vocab, page_cap,
+                                       tokens, seq_len, (const float*)c->embed, c->inv_freq,
+                                       c->pos_phys, c->seq_snap, c->ncommit, (float*)c->x,
+                                       c->cosb, c->sinb, c->err, st));
+  Commit cm;
+  cm.n = c->ncommit; cm.base = c->seq_snap; cm.page_table = page_table;
+  cm.num_pages = num_pages;
+  const bool fuse = g.dtype == WEDLM_BF16;
+  for (int l = 0; l < g.n_layers; ++l) {
+    void* wl = (char*)c->kv_win + (size_t)l * c->win_layer_stride * c->es;
+    const void* next_norm = fuse && l + 1 < g.n_layers ? c->layers[l + 1].attn_norm : nullptr;
+    const int rc =
+        fuse ? layer_impl<bf16>(c, l, batch, win, (bf16*)c->x, c->seq_snap, page_table,
+                                num_pages, kv_pools[l], wl, st, l > 0, next_norm, cm)
+             : layer_impl<float>(c, l, batch, win, (float*)c->x, c->seq_snap, page_table,
+                                 num_pages, kv_pools[l], wl, st, false, nullptr, cm);
+    if (rc) return rc;
+  }
+  LAUNCH(c, WEDLM_KIND_SELECT, st, launch_seq_advance(batch, chunk, c->seq_snap, seq_len, st));
+  if (hidden)
+    CUDA_TRY(c, cudaMemcpyAsync(hidden, c->x, (size_t)M * g.hidden * c->es,
+                                cudaMemcpyDeviceToDevice, st));
+  return WEDLM_OK;
+}
+
+int wedlm_generate(wedlm_ctx* c, const wedlm_gen_in* in, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  int rc = check_gen_args(c, in);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  if (in->max_steps == 0) return WEDLM_OK;
+  std::vector<uint64_t> key = gen_key(c, in);
+  GraphEntry* hit = nullptr;
+  for (auto& e : c->gen_graphs)
+    if (e.key == key) hit = &e;
+  if (!hit) {
+    cudaGraphExec_t exec = nullptr;
+    if ((rc = build_gen_graph(c, in, &exec))) return rc;
+    if ((int)c->gen_graphs.size() >= kMaxGraphs) {
+      auto lru = std::min_element(c->gen_graphs.begin(), c->gen_graphs.end(),
+                                  [](const GraphEntry& a, const GraphEntry& b) {
+                                    return a.last_use < b.last_use;
+                                  });
+      cudaGraphExecDestroy(lru->exec);
+      c->gen_graphs.erase(lru);
+    }
+    c->gen_graphs.push_back(GraphEntry{key, exec, 0});
+    hit = &c->gen_graphs.back();
+  }
+  hit->last_use = ++c->graph_clock;
+  CUDA_TRY(c, cudaGraphLaunch(hit->exec, st));
+  return WEDLM_OK;
+}
+
+int wedlm_dual_stream_attention(wedlm_ctx* c, int32_t n, int32_t block, const void* q,
+                                const void* mem_pool, const void* win, void* o, void* stream) {
+  if (!c) return WEDLM_ERR_INVALID_ARG;
+  const wedlm_config& g = c->cfg;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
+  if (g.dtype != WEDLM_BF16 || block < 16 || block % kPageBlock || n < block || n % block ||
+      !q || !mem_pool || !win || !o || misaligned(q) || misaligned(mem_pool) ||
+      misaligned(win) || misaligned(o))
+    return fail(c, WEDLM_ERR_INVALID_ARG, "bad dual-stream arguments");
+  int rpb = 0;
+  const int nrb = attention_tc_row_blocks(g.n_q_heads, g.n_kv_heads, block, &rpb);
+  if (nrb == 0) return fail(c, WEDLM_ERR_INVALID_ARG, "block too large for the attention");
+  const int nb = n / block, B = 2 * nb, n_pages = n / kPageBlock;
+  const size_t units = (size_t)B * g.n_kv_heads * nrb;
+  if (B > kDualMaxBlocks || n_pages > kDualMaxPages || units > c->attn_units_cap ||
+      ((size_t)c->num_sms + units) * rpb > c->attn_part_rows)
+    return fail(c, WEDLM_ERR_CAPACITY, "dual-stream shape beyond the context's workspace");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  dual_setup_kernel<<<std::max(1, (std::max(B, n_pages) + 255) / 256), 256, 0, st>>>(
+      nb, block, n_pages, c->dual_len, c->dual_pt);
+  CUDA_TRY(c, cudaGetLastError());
+  AttnArgs A = attn_args(c, B, chunk_win(block), q, mem_pool, c->dual_pt, c->dual_len, n_pages,
+                         win, o);
+  A.max_pages = n_pages;
+  A.pt_stride = 0;  // every block reads the one identity row
+  cudaError_t e;
+  {
+    Timed t(c, WEDLM_KIND_ATTN, st);
+    // plain launch: the lengths and the page row come from the kernel above
+    e = launch_attention_tc(A, c->zero_page, c->num_sms, st, false);
+  }
+  if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
+  return WEDLM_OK;
+}
+
 int wedlm_reorder_embed(wedlm_ctx* c, int32_t batch, const int32_t* tokens,
                         const int32_t* pos, const uint8_t* observed, int32_t* perm,
                         int32_t* inv, void* x_out, int32_t* pos_phys, void* stream) {
@@ -704,15 +1040,15 @@ int wedlm_reorder_embed(wedlm_ctx* c, int32_t batch, const int32_t* tokens,
                                    g.max_pages_per_seq * kPageBlock, tokens, pos,
                                    observed, c->ncommit, nullptr, (const bf16*)c->embed,
                                    c->inv_freq, c->perm, c->inv, c->pos_phys,
-                                   c->seq_snap, nullptr, (bf16*)x_out, c->cosb,
-                                   c->sinb, c->err, st);
+                                   c->seq_snap, nullptr, nullptr, nullptr, (bf16*)x_out,
+                                   c->cosb, c->sinb, c->err, st);
   else
     e = launch_reorder_embed<float>(batch, g.window, g.hidden, g.head_dim, g.vocab,
                                     g.max_pages_per_seq * kPageBlock, tokens, pos,
                                     observed, c->ncommit, nullptr, (const float*)c->embed,
                                     c->inv_freq, c->perm, c->inv, c->pos_phys,
-                                    c->seq_snap, nullptr, (float*)x_out, c->cosb,
-                                    c->sinb, c->err, st);
+                                    c->seq_snap, nullptr, nullptr, nullptr, (float*)x_out,
+                                    c->cosb, c->sinb, c->err, st);
   if (e != cudaSuccess) return fail(c, WEDLM_ERR_CUDA, cudaGetErrorString(e));
   if (perm) CUDA_TRY(c, cudaMemcpyAsync(perm, c->perm, M * 4, cudaMemcpyDeviceToDevice, st));
   if (inv) CUDA_TRY(c, cudaMemcpyAsync(inv, c->inv, M * 4, cudaMemcpyDeviceToDevice, st));
@@ -738,10 +1074,10 @@ int wedlm_layer(wedlm_ctx* c, int32_t layer, int32_t batch, void* x,
                               cudaMemcpyDeviceToDevice, st));
   void* win = (char*)c->kv_win + (size_t)layer * c->win_layer_stride * c->es;
   int rc = g.dtype == WEDLM_BF16
-               ? layer_impl<bf16>(c, layer, batch, (bf16*)c->x, seq_len, page_table,
+               ? layer_impl<bf16>(c, layer, batch, ctx_win(c), (bf16*)c->x, seq_len, page_table,
                                   num_pages, kv_pool, win, st)
-               : layer_impl<float>(c, layer, batch, (float*)c->x, seq_len, page_table,
-                                   num_pages, kv_pool, win, st);
+               : layer_impl<float>(c, layer, batch, ctx_win(c), (float*)c->x, seq_len,
+                                   page_table, num_pages, kv_pool, win, st);
   if (rc) return rc;
   CUDA_TRY(c, cudaMemcpyAsync(x, c->x, (size_t)M * g.hidden * c->es,
                               cudaMemcpyDeviceToDevice, st));
@@ -765,7 +1101,8 @@ int wedlm_attention(wedlm_ctx* c, int32_t batch, const void* q, const void* kv_p
     return fail(c, WEDLM_ERR_INVALID_ARG, "bad attention arguments");
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
-  AttnArgs A = attn_args(c, batch, q, kv_pool, page_table, seq_len, num_pages, kv_win, o);
+  AttnArgs A = attn_args(c, batch, ctx_win(c), q, kv_pool, page_table, seq_len, num_pages,
+                         kv_win, o);
   cudaError_t e;
   {
     Timed t(c, WEDLM_KIND_ATTN, st);

@@ -106,9 +106,17 @@ __device__ void run_epilogue(const GemmEpi& e, const float* sacc, int m0,
           const int kvh = gh - e.nq - (kind == 2 ? e.nkv : 0);
           T* blk = static_cast<T*>(e.kv_win) +
                    (((size_t)b * 2 + (kind - 1)) * e.nkv + kvh) * e.Wp * hd;
+          // a committed row (physical rows 0..c-1) also goes to its page
+          const bool commit = e.commit_n && p < e.commit_n[b];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            if (i < per) blk[tile_off(p, lane + 32 * i, hd)] = from_f<T>(v[i]);
+            if (i < per) {
+              blk[tile_off(p, lane + 32 * i, hd)] = from_f<T>(v[i]);
+              if (commit) {
+                T* c = commit_dst<T>(e, b, e.commit_base[b] + p, kind - 1, kvh, lane + 32 * i);
+                if (c) *c = from_f<T>(v[i]);
+              }
+            }
         }
       }
     }

@@ -131,10 +131,13 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
       }
       const bf16* gw = static_cast<const bf16*>(kind == 0 ? e.q_norm : e.k_norm);
       bf16* dst;
+      const int kvh = kind == 0 ? 0 : gh - e.nq - (kind == 2 ? e.nkv : 0);
+      // committed rows (physical rows 0..c-1) also go to their page
+      const bool commit = kind > 0 && a.valid && e.commit_n && p < e.commit_n[b];
+      const int t_commit = commit ? e.commit_base[b] + p : 0;
       if (kind == 0) {
         dst = static_cast<bf16*>(e.q_out) + ((size_t)m * e.nq + gh) * hd;
       } else {
-        const int kvh = gh - e.nq - (kind == 2 ? e.nkv : 0);
         dst = static_cast<bf16*>(e.kv_win) +
               (((size_t)b * 2 + (kind - 1)) * e.nkv + kvh) * e.Wp * hd;
       }
@@ -184,6 +187,12 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
             }
             st16(dst + tile_off(p, c + 8 * j8, hd), o1);
             st16(dst + tile_off(p, hh + c + 8 * j8, hd), o2);
+            if (commit) {
+              bf16* c1 = commit_dst<bf16>(e, b, t_commit, kind - 1, kvh, c + 8 * j8);
+              bf16* c2 = commit_dst<bf16>(e, b, t_commit, kind - 1, kvh, hh + c + 8 * j8);
+              if (c1) st16(c1, o1);
+              if (c2) st16(c2, o2);
+            }
           }
         }
       }

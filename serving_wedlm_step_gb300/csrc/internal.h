@@ -6,12 +6,31 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
 
 namespace wedlm {
+
+// Raise a kernel's dynamic shared-memory limit on the current device.  The
+// attribute belongs to (kernel, device): it is set once per pair, under a
+// lock, so launches on a second device (or from several threads) see it too.
+inline cudaError_t ensure_dyn_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
 
 // Launch with programmatic stream serialization (see pdl_wait): the kernel
 // must call pdl_wait before touching the previous kernel's results.
@@ -37,6 +56,28 @@ constexpr int kNormThreads = 512;
 
 enum EpiMode { EPI_RESID = 0, EPI_SWIGLU = 1, EPI_QKV = 2, EPI_LMHEAD = 3 };
 
+#ifdef __CUDACC__
+// Element (token t % 16, dim d) of K (kv = 0) or V (kv = 1), kv head kvh,
+// of the page holding position t of sequence b, for a committed window row;
+// null when the position is beyond the page table or its page id is out of
+// range (the error word records which).
+template <typename T, typename Epi>
+__device__ __forceinline__ T* commit_dst(const Epi& e, int b, int t, int kv, int kvh, int d) {
+  const int pg = t / kPageBlock;
+  if (pg >= e.max_pages) {
+    set_err(e.err, WEDLM_DEV_CAPACITY);
+    return nullptr;
+  }
+  const int page = e.page_table[(size_t)b * e.max_pages + pg];
+  if (page < 0 || page >= e.num_pages) {
+    set_err(e.err, WEDLM_DEV_BAD_PAGE);
+    return nullptr;
+  }
+  return static_cast<T*>(e.pool) + (((size_t)page * 2 + kv) * e.nkv + kvh) * kPageBlock * e.hd +
+         tile_off(t % kPageBlock, d, e.hd);
+}
+#endif
+
 // Epilogue of the weight-streaming GEMM Y[m][n] = sum_k X[m][k] W[n][k].
 struct GemmEpi {
   int mode;
@@ -53,6 +94,15 @@ struct GemmEpi {
   const void* k_norm;
   int qk_norm, W, Wp, nq, nkv, hd;
   float eps;
+  // QKV, commit into the paged cache: window row p of sequence b with
+  // p < commit_n[b] (the leftmost observed run, physical rows 0..c-1) also
+  // writes its K and V at position commit_base[b] + p of `pool`
+  const int32_t* commit_n;     // [B] or null (nothing committed)
+  const int32_t* commit_base;  // [B]
+  const int32_t* page_table;   // [B][max_pages]
+  void* pool;                  // this layer's KV pool
+  int max_pages, num_pages;
+  int* err;
   // LMHEAD
   SoftmaxPart* part;    // [tiles][M]
   int mask_id, vocab;
@@ -81,6 +131,8 @@ struct GemmProblem {
 
 struct AttnArgs {
   int B, W, Wp, nq, nkv, hd, chunk, max_chunks, num_pages, max_pages;
+  int pt_stride;        // page-table row of sequence b starts at b * pt_stride
+                        // (max_pages; 0: every sequence reads row 0)
   float scale_log2;     // log2(e) / sqrt(hd)
   const void* q;        // [B*W][nq][hd]
   const void* pool;     // this layer's pool
@@ -111,8 +163,17 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  const T* embed, const double* inv_freq,
                                  int32_t* perm_ws, int32_t* inv_ws,
                                  int32_t* pos_phys, int32_t* seq_snap,
+                                 int32_t* ncommit, const int32_t* done,
                                  int32_t* plant_phys, T* x, float* cosb,
                                  float* sinb, int* err, cudaStream_t st);
+template <typename T>
+cudaError_t launch_prefill_embed(int B, int C, int H, int hd, int vocab, int page_cap,
+                                 const int32_t* tokens, const int32_t* seq_len, const T* embed,
+                                 const double* inv_freq, int32_t* pos_phys, int32_t* seq_snap,
+                                 int32_t* ncommit, T* x, float* cosb, float* sinb, int* err,
+                                 cudaStream_t st);
+cudaError_t launch_seq_advance(int B, int C, const int32_t* seq_snap, int32_t* seq_len,
+                               cudaStream_t st);
 cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
                               const double* inv_freq, float* cosb, float* sinb,
                               cudaStream_t st);
@@ -125,19 +186,36 @@ template <typename T>
 cudaError_t launch_attention(const AttnArgs& A, cudaStream_t st);
 template <typename T>
 cudaError_t launch_attention_merge(const AttnArgs& A, cudaStream_t st);
-// tensor-core attention (bf16, head_dim 128, G*W <= 128, W <= 64) and its
-// segment merge (two kernels); grid = blocks (one per SM); zero_page: 4 KiB
-// of zeros in device memory.  part_o / part_ml must hold grid + B*nkv
-// segments of G*W rows.
+// tensor-core attention (bf16, head_dim 128; the segment merge is inside);
+// grid = blocks (one per SM); zero_page: 4 KiB of zeros in device memory.
+// The G*W query rows of a kv head run in row blocks of at most 128 rows
+// (attention_tc_row_blocks gives their number, or 0 for an unsupported
+// shape, and the rows per block); part_o / part_ml must hold
+// grid + B*nkv*row_blocks segments of rows_per_block rows and unit_cnt
+// B*nkv*row_blocks counters.
 cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
-                                cudaStream_t st);
+                                cudaStream_t st, bool pdl = true);
+int attention_tc_row_blocks(int nq, int nkv, int W, int* rows_per_block);
 cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 wedlm_slot_rec* rows, int* err,
                                 cudaStream_t st);
 
+enum ScoreMode { SCORE_ENTROPY = 0, SCORE_NEGLOGP = 1 };
+
 struct SelArgs {
   int B, W, mask_id;
   float alpha, tau;
+  int score_mode;             // ScoreMode
+  // streaming generation (all optional): done[b] = 1 marks a stopped
+  // sequence (left unchanged); a sequence stops once seq_len reaches
+  // stop_len[b] or after committing stop_token; committed tokens are also
+  // written to out_tokens[b][pos - out_base[b]] when 0 <= that < out_cap
+  int32_t* done;
+  const int32_t* stop_len;
+  int stop_token;
+  int32_t* out_tokens;
+  const int32_t* out_base;
+  int out_cap;
   const int32_t* tokens;
   const int32_t* pos;
   const uint8_t* obs;
@@ -150,7 +228,7 @@ struct SelArgs {
   uint8_t* new_obs;
   int32_t* committed;
   int32_t* n_committed;
-  int32_t* ncommit_ws;
+  const int32_t* ncommit_ws;  // commit counts found at step start (reorder)
   uint8_t* filled;
 };
 cudaError_t launch_select(const SelArgs& S, cudaStream_t st);

@@ -56,10 +56,12 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
                                       const int32_t* page_table, const int32_t* seq_len,
                                       const void* kv_win, void* o, void* stream) {
   const int hd = 128;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
   if (batch < 1 || window < 1 || window > kMaxWindow || n_kv_heads < 1 ||
-      n_q_heads % n_kv_heads || (n_q_heads / n_kv_heads) * window > 128 ||
-      max_pages_per_seq < 1 || num_pages < 1 || !q || !kv_pool || !page_table || !seq_len ||
-      !kv_win || !o)
+      n_q_heads < n_kv_heads || n_q_heads % n_kv_heads ||
+      (n_q_heads / n_kv_heads) * window > 128 || max_pages_per_seq < 1 || num_pages < 1 ||
+      !q || !kv_pool || !page_table || !seq_len || !kv_win || !o || misaligned(q) ||
+      misaligned(kv_pool) || misaligned(kv_win) || misaligned(o))
     return WEDLM_ERR_INVALID_ARG;
   const int Wp = ((window + kPageBlock - 1) / kPageBlock) * kPageBlock;
   const int R = (n_q_heads / n_kv_heads) * window;
@@ -90,7 +92,7 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
 
   AttnArgs A{};
   A.B = batch; A.W = window; A.Wp = Wp; A.nq = n_q_heads; A.nkv = n_kv_heads; A.hd = hd;
-  A.num_pages = num_pages; A.max_pages = max_pages_per_seq;
+  A.num_pages = num_pages; A.max_pages = max_pages_per_seq; A.pt_stride = max_pages_per_seq;
   A.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128)
   A.q = q; A.pool = kv_pool; A.page_table = page_table; A.seq_len = seq_len;
   A.kv_win = kv_win; A.part_o = part_o; A.part_ml = part_ml; A.o = o;

@@ -6,17 +6,23 @@
 // physical order) attend to every cached prefix position and, causally, to
 // the window (§3.2).
 //
-// Work = unit (sequence b, kv head) x 128-key tiles: ceil(L_b/128) prefix
-// tiles, then one window tile.  Stream-K: the units' tiles are laid end to
-// end and every block (one per SM) takes an equal contiguous share, so a
-// block processes runs ("segments") of consecutive tiles of one unit.  A
-// unit inside one block is normalised and written out directly; otherwise
-// each segment writes an unnormalised partial (O, running max, row sum) and
-// the block that finishes a unit's last segment (a per-unit counter) merges
-// the partials and writes the output.
+// The G*W query rows of a kv head (row r = p*G + g for window row p, q head
+// g: the order in which one TMA box {8 dims, G heads, tokens} of q lands in
+// shared memory) are cut into row blocks of at most 128 rows, the MMA's M:
+// one block of all G*W rows when they fit, else blocks of TPB = 128/G window
+// rows (prefill chunks, W = 64 at G = 4).
 //
-// Row r of a unit is (window row p, q head g) with r = p*G + g: the order in
-// which one TMA box {8 dims, G heads, W tokens} of q lands in shared memory.
+// Work = unit (sequence b, kv head, row block rb) x 128-key tiles:
+// ceil(L_b/128) prefix tiles, then the window tiles the row block's causal
+// extent reaches (window rows < (rb+1)*TPB).  Stream-K: the units' tiles are
+// laid end to end and every block (one per SM) takes an equal contiguous
+// share, so a block processes runs ("segments") of consecutive tiles of one
+// unit; the row blocks of one kv head are adjacent, so blocks running side
+// by side read the same cached pages and the second read hits L2.  A unit
+// inside one block is normalised and written out directly; otherwise each
+// segment writes an unnormalised partial (O, running max, row sum) and the
+// block that finishes a unit's last segment (a per-unit counter) merges the
+// partials and writes the output.
 //
 // Data path of one tile i (everything the softmax warps and the MMA issuers
 // hand each other lives in TMEM):
@@ -76,12 +82,18 @@ constexpr int kMaxGrid = 256;              // blocks of one launch
 constexpr uint32_t kDynBytes = 205 * 1024; // dynamic shared memory (+1 KiB align)
 }  // namespace
 
-// ring depths and shared-memory carve-up of one launch (host-chosen)
+constexpr int kMaxRB = 32;  // row blocks per kv head
+
+// ring depths, row blocks and shared-memory carve-up of one launch
+// (host-chosen)
 struct AttnLayout {
-  int R, Rpad;          // rows of a unit, rounded up to 8
+  int R, Rpad;          // rows of a row block (<= 128), rounded up to 8
   int KS, VS;           // K and V ring depths
   uint32_t q_bytes;     // one Q buffer: 16 dim groups x Rpad rows x 16 B
   uint32_t off_k, off_v;
+  int TPB, NRB;         // window rows per row block, row blocks per kv head
+  int wt[kMaxRB];       // window tiles of row block rb
+  int cwt[kMaxRB + 1];  // their prefix sums
 };
 
 // Split of the flattened tile sequence over the blocks; every block and the
@@ -105,8 +117,9 @@ __device__ __forceinline__ int last_le(const long long* a, int n, long long x) {
 __device__ __forceinline__ int seq_len_clamped(const AttnArgs& A, int b) {
   return max(0, min(A.seq_len[b], A.max_pages * kPageBlock));
 }
-__device__ __forceinline__ int seq_tiles(const AttnArgs& A, int b) {
-  return (seq_len_clamped(A, b) + kTile - 1) / kTile + 1;
+// prefix tiles of sequence b
+__device__ __forceinline__ int prefix_tiles(const AttnArgs& A, int b) {
+  return (seq_len_clamped(A, b) + kTile - 1) / kTile;
 }
 
 __device__ __forceinline__ uint32_t idesc_pv() {  // M=128, N=128, B MN-major
@@ -194,12 +207,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   __shared__ float s_lsum[2][128];        // [half][row]: segment row sums
   __shared__ long long s_tstart[kMaxB + 1];    // first global tile of sequence b
   __shared__ long long s_begin[kMaxGrid + 1];  // first global tile of block c
-  __shared__ int s_T[kMaxB];                   // tiles of one unit of sequence b
+  __shared__ int s_P[kMaxB];                   // prefix tiles of sequence b
   __shared__ int s_pages[kPrefTiles * kPagesPerTile];  // page ids (-1: none)
   __shared__ StreamSplit s_split;
 
   const int hd = 128, G = A.nq / A.nkv, W = A.W, R = Ly.R;
-  const int KS = Ly.KS, VS = Ly.VS;
+  const int KS = Ly.KS, VS = Ly.VS, NRB = Ly.NRB, TPB = Ly.TPB;
+  // tiles of all row blocks of one kv head of a sequence with P prefix tiles
+  auto head_tiles = [&](int P) { return NRB * P + Ly.cwt[NRB]; };
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,13 +224,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   // (the tiles of unit u inside block c) has slot u + c: along the tile
   // order neither u nor c ever decreases and one of them grows from one
   // segment to the next, so slots are distinct and fewer than units + G.
-  for (int b = threadIdx.x; b < A.B; b += kThreads) s_T[b] = seq_tiles(A, b);
+  for (int b = threadIdx.x; b < A.B; b += kThreads) s_P[b] = prefix_tiles(A, b);
   __syncthreads();
   if (warp == 0) {
     const int per = (A.B + 31) / 32;
     const int b0 = min(A.B, lane * per), b1 = min(A.B, b0 + per);
     long long sum = 0;
-    for (int b = b0; b < b1; ++b) sum += (long long)s_T[b] * A.nkv;
+    for (int b = b0; b < b1; ++b) sum += (long long)head_tiles(s_P[b]) * A.nkv;
     long long incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -225,7 +240,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     long long acc = incl - sum;
     for (int b = b0; b < b1; ++b) {
       s_tstart[b] = acc;
-      acc += (long long)s_T[b] * A.nkv;
+      acc += (long long)head_tiles(s_P[b]) * A.nkv;
     }
     if (lane == 31) {
       StreamSplit sp;
@@ -275,42 +290,55 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
 
   const long long g0 = s_begin[blockIdx.x];
   const int ntiles = (int)(s_begin[blockIdx.x + 1] - g0);
-  // position of a block tile: sequence, kv head, tile within the unit and
-  // tiles of the unit; found once, then advanced tile by tile
-  struct Cur { int b, kvh, t, T, L; };
-  Cur first;
-  {
-    first.b = last_le(s_tstart, A.B, g0);
-    first.L = seq_len_clamped(A, first.b);
-    first.T = s_T[first.b];
-    const long long off = g0 - s_tstart[first.b];
-    first.kvh = (int)(off / first.T);
-    first.t = (int)(off % first.T);
-  }
+  // position of a tile: sequence, kv head, row block, tile within the unit
+  // (prefix tiles 0..P-1, then window tiles), tiles of the unit, cached
+  // length and prefix tiles of the sequence; found by search for a block's
+  // first tile, then advanced tile by tile
+  struct Cur { int b, kvh, rb, t, T, L, P; };
+  auto locate = [&](long long g) {
+    Cur c;
+    c.b = last_le(s_tstart, A.B, g);
+    c.L = seq_len_clamped(A, c.b);
+    c.P = s_P[c.b];
+    const long long off = g - s_tstart[c.b];
+    const int TS = head_tiles(c.P);
+    c.kvh = (int)(off / TS);
+    const int r = (int)(off % TS);
+    c.rb = 0;
+    while (c.rb + 1 < NRB && (c.rb + 1) * c.P + Ly.cwt[c.rb + 1] <= r) ++c.rb;
+    c.t = r - (c.rb * c.P + Ly.cwt[c.rb]);
+    c.T = c.P + Ly.wt[c.rb];
+    return c;
+  };
+  const Cur first = locate(g0);
   auto advance = [&](Cur& c) {
     if (++c.t == c.T) {
       c.t = 0;
-      if (++c.kvh == A.nkv) {
-        c.kvh = 0;
-        if (c.b + 1 < A.B) {
-          c.L = seq_len_clamped(A, ++c.b);
-          c.T = s_T[c.b];
+      if (++c.rb == NRB) {
+        c.rb = 0;
+        if (++c.kvh == A.nkv) {
+          c.kvh = 0;
+          if (c.b + 1 < A.B) {
+            c.L = seq_len_clamped(A, ++c.b);
+            c.P = s_P[c.b];
+          }
         }
       }
+      c.T = c.P + Ly.wt[c.rb];
     }
   };
+  // keys of window tile w (the last one may be partial: Wp is a multiple of 16)
+  auto window_keys = [&](int w) { return min(kTile, A.Wp - w * kTile); };
 
   // page ids of the block's first kPrefTiles tiles, loaded and checked by
   // every thread at once so the copiers never wait on a global load
   for (int e = threadIdx.x; e < min(ntiles, kPrefTiles) * kPagesPerTile; e += kThreads) {
-    const long long g = g0 + e / kPagesPerTile;
-    const int b = last_le(s_tstart, A.B, g);
-    const int L = seq_len_clamped(A, b), T = s_T[b];
-    const int t = (int)((g - s_tstart[b]) % T);
+    const Cur c = locate(g0 + e / kPagesPerTile);
+    const int b = c.b, L = c.L, t = c.t;
     const int t0 = t * kTile + (e % kPagesPerTile) * kPageBlock;
     int pid = -1;
-    if (t != T - 1 && t0 < L) {
-      pid = A.page_table[(size_t)b * A.max_pages + t0 / kPageBlock];
+    if (t < c.P && t0 < L) {
+      pid = A.page_table[(size_t)b * A.pt_stride + t0 / kPageBlock];
       if (pid < 0 || pid >= A.num_pages) {
         set_err(A.err, WEDLM_DEV_BAD_PAGE);
         pid = -1;
@@ -333,14 +361,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       if (!kv) tma_prefetch_desc(&mq);
       // a new segment's Q goes into buffer seg & 1 once the S MMAs of the
       // segment two back are done with it
-      auto issue_q = [&](int sg, int b, int kvh) -> bool {
+      auto issue_q = [&](int sg, int b, int kvh, int rb) -> bool {
         const int qb = sg & 1;
         if (!wait(&q_empty[qb], ((uint32_t)(sg >> 1) & 1u) ^ 1u)) return false;
         uint8_t* qdst = base + qb * Ly.q_bytes;
         mbar_arrive_expect_tx(&q_full[qb], (uint32_t)(16 * R * 16));
 #pragma unroll 1
         for (int c = 0; c < 16; ++c)
-          tma_load_3d(qdst + c * Ly.Rpad * 16, &mq, &q_full[qb], 8 * c, kvh * G, b * W);
+          tma_load_3d(qdst + c * Ly.Rpad * 16, &mq, &q_full[qb], 8 * c, kvh * G,
+                      b * W + rb * TPB);
         s_issued[2] = sg + 1;
         return true;
       };
@@ -348,29 +377,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       // projection): the first ring of prefix tiles is copied before
       // waiting for it; Q and the window tile (both its outputs) after.
       bool waited = false;
-      int nq_def = 0, qdef_seg[kMaxStages], qdef_b[kMaxStages], qdef_h[kMaxStages];
+      int nq_def = 0, qdef_seg[kMaxStages], qdef_b[kMaxStages], qdef_h[kMaxStages],
+          qdef_rb[kMaxStages];
       auto wait_prev = [&]() -> bool {
         pdl_wait();
         if (!kv) pdl_trigger();
         waited = true;
         for (int j = 0; j < nq_def; ++j)
-          if (!issue_q(qdef_seg[j], qdef_b[j], qdef_h[j])) return false;
+          if (!issue_q(qdef_seg[j], qdef_b[j], qdef_h[j], qdef_rb[j])) return false;
         nq_def = 0;
         return true;
       };
       int seg = -1;
       Cur cur = first;
       for (int i = 0; i < ntiles; ++i, advance(cur)) {
-        const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
-        if (!waited && (i == NS || t == T - 1) && !wait_prev()) break;
+        const int b = cur.b, kvh = cur.kvh, t = cur.t;
+        const bool window = t >= cur.P;
+        if (!waited && (i == NS || window) && !wait_prev()) break;
         if (!kv && (i == 0 || t == 0)) {
           ++seg;
           if (waited) {
-            if (!issue_q(seg, b, kvh)) break;
+            if (!issue_q(seg, b, kvh, cur.rb)) break;
           } else {
             qdef_seg[nq_def] = seg;
             qdef_b[nq_def] = b;
             qdef_h[nq_def] = kvh;
+            qdef_rb[nq_def] = cur.rb;
             ++nq_def;
           }
         }
@@ -382,8 +414,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
           } else {
             const int t0 = t * kTile + pg * kPageBlock;
             int v = -1;
-            if (t != T - 1 && t0 < cur.L) {
-              v = A.page_table[(size_t)b * A.max_pages + t0 / kPageBlock];
+            if (!window && t0 < cur.L) {
+              v = A.page_table[(size_t)b * A.pt_stride + t0 / kPageBlock];
               if (v < 0 || v >= A.num_pages) {
                 set_err(A.err, WEDLM_DEV_BAD_PAGE);
                 v = -1;
@@ -397,11 +429,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         uint64_t* full = kv ? &v_full[st] : &k_full[st];
         if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
         uint8_t* dst = base + (kv ? Ly.off_v : Ly.off_k) + st * kKVBytes;
-        if (t == T - 1) {
-          const uint32_t bytes = (uint32_t)A.Wp * hd * 2;
+        if (window) {
+          const int w = t - cur.P;
+          const uint32_t bytes = (uint32_t)window_keys(w) * hd * 2;
           mbar_arrive_expect_tx(full, bytes);
-          bulk_load(dst, win + (((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp * hd, bytes, full,
-                    pol);
+          bulk_load(dst, win + ((((size_t)b * 2 + kv) * A.nkv + kvh) * A.Wp + (size_t)w * kTile) * hd,
+                    bytes, full, pol);
         } else {
           mbar_arrive_expect_tx(full, kKVBytes);
 #pragma unroll
@@ -430,6 +463,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       for (int i = 0; i < ntiles; ++i, advance(cs)) {
         const int t = cs.t, T = cs.T;
         const bool seg_first = (i == 0 || t == 0), seg_last = (i == ntiles - 1 || t == T - 1);
+        const int keys = t >= cs.P ? window_keys(t - cs.P) : kTile;
         if (seg_first) {
           ++seg;
           if (!wait(&q_full[seg & 1], (uint32_t)(seg >> 1) & 1u)) break;
@@ -443,7 +477,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         tc_fence_after();
         const uint64_t aq = (seg & 1) ? dq1 : dq0;
         const uint64_t bk = dk0 + (uint64_t)((st * kKVBytes) >> 4);
-        const uint32_t idS = idesc_bf16_m128(t == T - 1 ? A.Wp : kTile);
+        const uint32_t idS = idesc_bf16_m128(keys);
         const uint32_t dS = tmem + kColS + (uint32_t)(sb * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // 16 dims a step: two 8-dim groups
@@ -461,7 +495,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       int seg = -1;
       Cur cp = first;
       for (int i = 0; i < ntiles; ++i, advance(cp)) {
-        const int t = cp.t, T = cp.T;
+        const int t = cp.t;
         const bool seg_first = (i == 0 || t == 0);
         const int st = i % VS, pb = i % kSBuf;
         if (!wait(&v_full[st], (uint32_t)(i / VS) & 1u)) break;
@@ -475,7 +509,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         tc_fence_after();
         const uint64_t bv = dv0 + (uint64_t)((st * kKVBytes) >> 4);
         const uint32_t ap = tmem + kColS + (uint32_t)(pb * 128);
-        const int steps = ((t == T - 1) ? A.Wp : kTile) / 16;
+        const int steps = (t >= cp.P ? window_keys(t - cp.P) : kTile) / 16;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)  // 16 keys a step: 8 TMEM columns of P
           if (kk < steps)
@@ -489,9 +523,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     // ---------------- softmax warps ----------------
     pdl_wait();  // they write the outputs (and read nothing else of the previous kernel)
     const int q = warp & 3, h = warp >> 2;       // lane quadrant, key / dim half
-    const int r = 32 * q + lane;                  // query row
-    const bool valid = r < R;
-    const int p_row = valid ? r / G : 0;          // window row of this query row
+    const int r = 32 * q + lane;                  // query row within the row block
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     const float sc = A.scale_log2;
     float m = -INFINITY, l = 0.f;
@@ -503,13 +535,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
     };
     Cur cur = first;
     for (int i = 0; i < ntiles; ++i, advance(cur)) {
-      const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T;
+      const int b = cur.b, kvh = cur.kvh, t = cur.t, T = cur.T, rb = cur.rb;
       const bool seg_first = (i == 0 || t == 0), seg_last = (i == ntiles - 1 || t == T - 1);
       if (seg_first) {
         m = -INFINITY;
         l = 0.f;
       }
-      const bool window = (t == T - 1);
+      // rows of this row block: window rows rb*TPB .. min(W, (rb+1)*TPB) - 1
+      const int rows_valid = (min(W, (rb + 1) * TPB) - rb * TPB) * G;
+      const bool valid = r < rows_valid;
+      const int p_row = rb * TPB + (valid ? r / G : 0);  // window row of this query row
+      const bool window = t >= cur.P;
       const int L = cur.L;
       const int sb = i % kSBuf;
       const uint32_t sph = (uint32_t)(i / kSBuf) & 1u;  // phase of this tile on buffer sb
@@ -519,12 +555,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       tmem_ld64(trow + kColS + (uint32_t)(sb * 128 + h * 64), v);
       // mask (only the partial last prefix tile and the window tile need
       // one), row max over both halves of the tile, scale applied once
-      const int kbase = t * kTile;
+      const int kbase = window ? (t - cur.P) * kTile : t * kTile;
       if (window || kbase + kTile > L) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          const int jj = h * 64 + j;
-          const bool ok = window ? (jj < W && jj <= p_row) : (kbase + jj < L);
+          const int kk = kbase + h * 64 + j;
+          const bool ok = window ? (kk < W && kk <= p_row) : (kk < L);
           if (!ok) v[j] = -INFINITY;
         }
       }
@@ -605,8 +641,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         const float lsum = l + s_lsum[h ^ 1][r];
         // the unit's segments: slots u + c for the blocks c from the owner
         // of its first tile to the owner of its last
-        const int u = b * A.nkv + kvh;
-        const long long u0 = s_tstart[b] + (long long)kvh * T;
+        const int u = (b * A.nkv + kvh) * NRB + rb;
+        const long long u0 = s_tstart[b] + (long long)kvh * head_tiles(cur.P) +
+                             (long long)rb * cur.P + Ly.cwt[rb];
         const int c0 = last_le(s_begin, sp.G, u0), c1 = last_le(s_begin, sp.G, u0 + T - 1);
         if (c0 == c1) {
           // the whole unit is in this block: normalise and write the output
@@ -658,7 +695,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
             const int nrg = (R + 31) / 32;
             for (int task = warp; task < nrg * 4; task += 8) {
               const int mr = 32 * (task % nrg) + lane, qd = task / nrg;
-              if (mr >= R) continue;
+              if (mr >= rows_valid) continue;
               const int hh = qd >> 1, d40 = (qd & 1) * 8;
               float M = -INFINITY, ls = 0.f, acc[32];
 #pragma unroll
@@ -706,7 +743,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
               }
               const float inv = ls > 0.f ? 1.f / ls : 0.f;
               bf16* dst = static_cast<bf16*>(A.o) +
-                          ((size_t)(b * W + mr / G) * A.nq + kvh * G + mr % G) * hd + qd * 32;
+                          ((size_t)(b * W + rb * TPB + mr / G) * A.nq + kvh * G + mr % G) * hd +
+                          qd * 32;
 #pragma unroll
               for (int j8 = 0; j8 < 4; ++j8) {
                 uint32_t w4[4];
@@ -759,15 +797,51 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encoder() {
 }
 }  // namespace
 
-cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
-                                cudaStream_t st) {
+// Row blocks of a launch: all G*W rows in one block when they fit the MMA's
+// 128 rows, else blocks of 128/G window rows (G must divide 128).  False for
+// shapes the kernel does not take.
+bool attention_tc_plan(const AttnArgs& A, AttnLayout* Ly) {
+  if (A.hd != 128 || A.nkv < 1 || A.nq % A.nkv || A.W < 1 ||
+      A.Wp != (A.W + kPageBlock - 1) / kPageBlock * kPageBlock)
+    return false;
   const int G = A.nq / A.nkv;
-  if (A.hd != 128 || G * A.W > 128 || A.Wp > 64 || A.B > kMaxB || A.min_tiles < 1 ||
-      !A.unit_cnt || grid < 1 || (reinterpret_cast<uintptr_t>(A.q) & 15))
-    return cudaErrorInvalidValue;
+  if (G > 128) return false;
+  if (G * A.W <= 128) {
+    Ly->TPB = A.W;
+  } else {
+    if (128 % G) return false;
+    Ly->TPB = 128 / G;
+  }
+  Ly->NRB = (A.W + Ly->TPB - 1) / Ly->TPB;
+  if (Ly->NRB > kMaxRB) return false;
+  Ly->R = G * Ly->TPB;
+  Ly->Rpad = (Ly->R + 7) / 8 * 8;
+  Ly->cwt[0] = 0;
+  for (int rb = 0; rb < Ly->NRB; ++rb) {
+    const int last = std::min(A.W, (rb + 1) * Ly->TPB) - 1;  // last window row of the block
+    Ly->wt[rb] = last / kTile + 1;
+    Ly->cwt[rb + 1] = Ly->cwt[rb] + Ly->wt[rb];
+  }
+  return true;
+}
+
+int attention_tc_row_blocks(int nq, int nkv, int W, int* rows_per_block) {
+  AttnArgs A{};
+  A.hd = 128; A.nq = nq; A.nkv = nkv; A.W = W;
+  A.Wp = (W + kPageBlock - 1) / kPageBlock * kPageBlock;
   AttnLayout Ly;
-  Ly.R = G * A.W;
-  Ly.Rpad = (Ly.R + 7) / 8 * 8;
+  if (!attention_tc_plan(A, &Ly)) return 0;
+  if (rows_per_block) *rows_per_block = Ly.R;
+  return Ly.NRB;
+}
+
+cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int grid,
+                                cudaStream_t st, bool pdl) {
+  AttnLayout Ly;
+  if (!attention_tc_plan(A, &Ly) || A.B > kMaxB || A.min_tiles < 1 || !A.unit_cnt || grid < 1 ||
+      (reinterpret_cast<uintptr_t>(A.q) & 15))
+    return cudaErrorInvalidValue;
+  const int G = A.nq / A.nkv;
   Ly.q_bytes = 256u * (uint32_t)Ly.Rpad;
   const int stages = (int)((kDynBytes - 2 * Ly.q_bytes) / kKVBytes);
   Ly.KS = stages >= 6 ? 3 : 2;
@@ -782,20 +856,19 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
   CUtensorMap mq;
   cuuint64_t dims[3] = {128, (cuuint64_t)A.nq, (cuuint64_t)A.B * A.W};
   cuuint64_t strides[2] = {128 * 2, (cuuint64_t)A.nq * 128 * 2};
-  cuuint32_t box[3] = {8, (cuuint32_t)G, (cuuint32_t)A.W};
+  cuuint32_t box[3] = {8, (cuuint32_t)G, (cuuint32_t)Ly.TPB};
   cuuint32_t estr[3] = {1, 1, 1};
   if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A.q), dims, strides, box,
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes + 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t ae = ensure_dyn_smem((const void*)attn_tc_kernel, (int)kDynBytes + 1024);
+  if (ae != cudaSuccess) return ae;
   const uint32_t smem = Ly.off_v + (uint32_t)Ly.VS * kKVBytes + 1024;
+  if (!pdl) {
+    attn_tc_kernel<<<std::min(grid, kMaxGrid), kThreads, smem, st>>>(mq, A, Ly, zero_page);
+    return cudaGetLastError();
+  }
   return launch_pdl(attn_tc_kernel, dim3(std::min(grid, kMaxGrid)), dim3(kThreads), smem, st, mq,
                     A, Ly, zero_page);
 }

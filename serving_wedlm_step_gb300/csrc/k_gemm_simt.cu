@@ -92,13 +92,8 @@ template <typename T>
 cudaError_t launch_gemm_simt(const GemmProblem& P, cudaStream_t st) {
   const int tiles = P.swiglu ? P.N / 128 : (P.N + 127) / 128;
   const size_t smem = (size_t)(BK * AS_LD + BK * XS_LD + 128 * 128) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gemm_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t ae = ensure_dyn_smem((const void*)gemm_simt_kernel<T>, (int)smem);
+  if (ae != cudaSuccess) return ae;
   gemm_simt_kernel<T><<<dim3(tiles, P.splits), 256, smem, st>>>(P);
   return cudaGetLastError();
 }

@@ -411,6 +411,8 @@ __global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
       for (int k = 0; k < 4; ++k) x[k] = x[k] * cs[k] + y[k] * sn[k];
     }
   }
+  const __nv_bfloat162 v01 = __floats2bfloat162_rn(x[0], x[1]);
+  const __nv_bfloat162 v23 = __floats2bfloat162_rn(x[2], x[3]);
   bf16* dst;
   if (kind == 0) {
     dst = static_cast<bf16*>(e.q_out) + ((size_t)m * e.nq + gh) * 128 + d0;
@@ -419,10 +421,19 @@ __global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
     const int kvh = gh - e.nq - (kind == 2 ? e.nkv : 0);
     dst = static_cast<bf16*>(e.kv_win) + (((size_t)b * 2 + (kind - 1)) * e.nkv + kvh) * e.Wp * 128 +
           tile_off(p, d0, 128);
+    // a committed row (physical rows 0..c-1) also goes to its page
+    if (e.commit_n && p < e.commit_n[b]) {
+      bf16* c = commit_dst<bf16>(e, b, e.commit_base[b] + p, kind - 1, kvh, d0);
+      if (c) {
+        __nv_bfloat162* cp = reinterpret_cast<__nv_bfloat162*>(c);
+        cp[0] = v01;
+        cp[1] = v23;
+      }
+    }
   }
   __nv_bfloat162* dp = reinterpret_cast<__nv_bfloat162*>(dst);
-  dp[0] = __floats2bfloat162_rn(x[0], x[1]);
-  dp[1] = __floats2bfloat162_rn(x[2], x[3]);
+  dp[0] = v01;
+  dp[1] = v23;
 }
 
 // any other epilogue: thread = (activation row, epilogue item)
@@ -540,8 +551,7 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
     return nullptr;
   }
   // dynamic shared memory: up to 220 KB of stages + 1 KB alignment slack
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxDynSmem);
+  cudaError_t e = ensure_dyn_smem((const void*)gemm_tc_kernel, kMaxDynSmem);
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (msg) *msg = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);

@@ -31,7 +31,8 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
                      const T* __restrict__ embed,
                      const double* __restrict__ inv_freq,
                      int32_t* perm_ws, int32_t* inv_ws, int32_t* pos_phys,
-                     int32_t* seq_snap, int32_t* plant_phys, T* x,
+                     int32_t* seq_snap, int32_t* ncommit,
+                     const int32_t* __restrict__ done, int32_t* plant_phys, T* x,
                      float* cosb, float* sinb, int* err) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
@@ -63,6 +64,17 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
       if (L < 0) { set_err(err, WEDLM_DEV_BAD_SEQLEN); L = 0; }
       if (L + W > page_cap) set_err(err, WEDLM_DEV_CAPACITY);
       seq_snap[b] = L;
+      // commit set (Method: the leftmost contiguous filled prefix): the
+      // run of slots 0..c-1 observed at input whose logical positions
+      // continue the committed prefix, pos = L + i.  Known before the
+      // forward, so the K/V of these rows go to their pages as they are
+      // computed.  A stopped sequence commits nothing.
+      int c = 0;
+      if (!(done && done[b])) {
+        const int32_t* ps = pos + (size_t)b * W;
+        while (c < W && o[c] && ps[c] == L + c) ++c;
+      }
+      if (ncommit) ncommit[b] = c;
     }
   }
   __syncthreads();
@@ -89,12 +101,78 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  const int32_t* seq_len, const int32_t* plant,
                                  const T* embed, const double* inv_freq,
                                  int32_t* perm_ws, int32_t* inv_ws,
-                                 int32_t* pos_phys, int32_t* seq_snap,
-                                 int32_t* plant_phys, T* x, float* cosb,
-                                 float* sinb, int* err, cudaStream_t st) {
+                                 int32_t* pos_phys, int32_t* seq_snap, int32_t* ncommit,
+                                 const int32_t* done, int32_t* plant_phys, T* x,
+                                 float* cosb, float* sinb, int* err, cudaStream_t st) {
   return launch_pdl(reorder_embed_kernel<T>, dim3(W, B), dim3(128), 0, st, W, H, hd, vocab,
                     page_cap, tokens, pos, obs, seq_len, plant, embed, inv_freq, perm_ws,
-                    inv_ws, pos_phys, seq_snap, plant_phys, x, cosb, sinb, err);
+                    inv_ws, pos_phys, seq_snap, ncommit, done, plant_phys, x, cosb, sinb, err);
+}
+
+// Prompt prefill rows (all observed, identity order): row p of sequence b
+// is chunk token p at logical position seq_len[b] + p; every row is
+// committed.  grid (C, B).
+template <typename T>
+__global__ void __launch_bounds__(128)
+prefill_embed_kernel(int C, int H, int hd, int vocab, int page_cap,
+                     const int32_t* __restrict__ tokens,
+                     const int32_t* __restrict__ seq_len, const T* __restrict__ embed,
+                     const double* __restrict__ inv_freq, int32_t* pos_phys,
+                     int32_t* seq_snap, int32_t* ncommit, T* x, float* cosb,
+                     float* sinb, int* err) {
+  pdl_wait();  // the previous kernel's results
+  pdl_trigger();
+  const int p = blockIdx.x, b = blockIdx.y, m = b * C + p;
+  int L = seq_len[b];
+  if (L < 0) {
+    if (threadIdx.x == 0 && p == 0) set_err(err, WEDLM_DEV_BAD_SEQLEN);
+    L = 0;
+  }
+  if (threadIdx.x == 0) {
+    pos_phys[m] = L + p;
+    if (p == 0) {
+      if (L + C > page_cap) set_err(err, WEDLM_DEV_CAPACITY);
+      seq_snap[b] = L;
+      ncommit[b] = C;
+    }
+  }
+  int tok = tokens[(size_t)b * C + p];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) set_err(err, WEDLM_DEV_BAD_TOKEN);
+    tok = 0;
+  }
+  const int half = hd / 2;
+  rope_row(L + p, half, inv_freq, cosb + (size_t)m * half, sinb + (size_t)m * half);
+  const uint4* src = reinterpret_cast<const uint4*>(embed + (size_t)tok * H);
+  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)m * H);
+  const int nv = H * (int)sizeof(T) / 16;
+  for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = src[i];
+}
+
+template <typename T>
+cudaError_t launch_prefill_embed(int B, int C, int H, int hd, int vocab, int page_cap,
+                                 const int32_t* tokens, const int32_t* seq_len, const T* embed,
+                                 const double* inv_freq, int32_t* pos_phys, int32_t* seq_snap,
+                                 int32_t* ncommit, T* x, float* cosb, float* sinb, int* err,
+                                 cudaStream_t st) {
+  return launch_pdl(prefill_embed_kernel<T>, dim3(C, B), dim3(128), 0, st, C, H, hd, vocab,
+                    page_cap, tokens, seq_len, embed, inv_freq, pos_phys, seq_snap, ncommit, x,
+                    cosb, sinb, err);
+}
+
+// seq_len[b] = seq_snap[b] + C once the chunk's K/V are in the pages
+__global__ void seq_advance_kernel(int B, int C, const int32_t* __restrict__ seq_snap,
+                                   int32_t* seq_len) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_len[b] = seq_snap[b] + C;
+}
+
+cudaError_t launch_seq_advance(int B, int C, const int32_t* seq_snap, int32_t* seq_len,
+                               cudaStream_t st) {
+  return launch_pdl(seq_advance_kernel, dim3((B + 127) / 128), dim3(128), 0, st, B, C, seq_snap,
+                    seq_len);
 }
 
 __global__ void rope_table_kernel(int hd, const int32_t* __restrict__ pos_phys,
@@ -164,10 +242,14 @@ cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
   template cudaError_t launch_reorder_embed<T>(                               \
       int, int, int, int, int, int, const int32_t*, const int32_t*,           \
       const uint8_t*, const int32_t*, const int32_t*, const T*, const double*, \
-      int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, T*, float*, float*,   \
-      int*, cudaStream_t);                                                    \
+      int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, const int32_t*,       \
+      int32_t*, T*, float*, float*, int*, cudaStream_t);                      \
   template cudaError_t launch_rmsnorm<T>(int, int, const T*, const T*, float, \
-                                         T*, cudaStream_t);
+                                         T*, cudaStream_t);                   \
+  template cudaError_t launch_prefill_embed<T>(                               \
+      int, int, int, int, int, int, const int32_t*, const int32_t*, const T*, \
+      const double*, int32_t*, int32_t*, int32_t*, T*, float*, float*, int*,  \
+      cudaStream_t);
 INST(float)
 INST(bf16)
 #undef INST

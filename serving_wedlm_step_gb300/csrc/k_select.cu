@@ -5,10 +5,13 @@
 // strict causality), picks additional masks to fill using
 // distance-penalized entropy H~_j = H_j + alpha*d_j (where d_j is distance
 // from slot j to the leftmost remaining mask), and refills the freed slots
-// with new [M] tokens".  Readings: score = entropy (nats); fill every masked
-// slot with H~ < tau, else the single argmin (ties: lowest slot, NaN =
-// +inf); d_j = pos_j - pos_m0 for the leftmost masked slot m0 at input;
-// commit = slots 0..c-1 observed at input with pos = L + i.
+// with new [M] tokens".  Readings: score = entropy (nats), or -ln p_max
+// for the confidence reading of the rule (Key claims §5.2 calls Eq. 11 a
+// "distance-penalized confidence rule"); fill every masked slot with
+// H~ < tau, else the single argmin (ties: lowest slot, NaN = +inf);
+// d_j = pos_j - pos_m0 for the leftmost masked slot m0 at input; commit =
+// slots 0..c-1 observed at input with pos = L + i (counted by the reorder
+// kernel at step start, when the K/V of those rows are written to pages).
 #include "internal.h"
 
 namespace wedlm {
@@ -87,33 +90,36 @@ __global__ void __launch_bounds__(kMaxWindow) select_kernel(SelArgs S) {
   __shared__ int s_obs[kMaxWindow], s_pos[kMaxWindow], s_tok[kMaxWindow];
   __shared__ int s_sel[kMaxWindow], s_fill_tok[kMaxWindow];
   __shared__ float s_ht[kMaxWindow];
-  __shared__ int s_m0, s_c;
+  __shared__ int s_m0, s_done;
   const int L = S.seq_snap[b];
+  // the window may be updated in place (out == in): everything is read
+  // into shared memory before anything is written
   if (j < W) {
     s_obs[j] = S.obs[b * W + j] != 0;
     s_pos[j] = S.pos[b * W + j];
     s_tok[j] = S.tokens[b * W + j];
   }
+  if (j == 0) s_done = S.done ? S.done[b] : 0;
   __syncthreads();
+  const bool stopped = s_done != 0;
+  const int c = stopped ? 0 : S.ncommit_ws[b];
   if (j == 0) {
     int m0 = -1;
     for (int i = 0; i < W; ++i)
       if (!s_obs[i]) { m0 = i; break; }
-    int c = 0;
-    while (c < W && s_obs[c] && s_pos[c] == L + c) ++c;
-    s_m0 = m0;
-    s_c = c;
+    s_m0 = stopped ? -1 : m0;
   }
   __syncthreads();
-  const int m0 = s_m0, c = s_c;
+  const int m0 = s_m0;
   if (j < W) {
     const wedlm_slot_rec rec = S.rows[b * W + S.inv[b * W + j]];
     s_fill_tok[j] = rec.argmax;
     float ht = __int_as_float(0x7fc00000);  // NaN at observed slots
     int sel = 0;
-    if (!s_obs[j]) {
+    if (!s_obs[j] && !stopped) {
       const float d = (float)(s_pos[j] - s_pos[m0]);
-      ht = __fadd_rn(rec.entropy, __fmul_rn(S.alpha, d));
+      const float score = S.score_mode == SCORE_NEGLOGP ? -logf(rec.p_max) : rec.entropy;
+      ht = __fadd_rn(score, __fmul_rn(S.alpha, d));
       sel = ht < S.tau;
     }
     s_ht[j] = ht;
@@ -152,11 +158,18 @@ __global__ void __launch_bounds__(kMaxWindow) select_kernel(SelArgs S) {
     S.new_obs[b * W + j] = (uint8_t)ob;
     S.committed[b * W + j] = j < c ? s_tok[j] : -1;
     if (S.filled) S.filled[b * W + j] = (uint8_t)s_sel[j];
+    if (S.out_tokens && j < c) {
+      const int k = L + j - S.out_base[b];
+      if (k >= 0 && k < S.out_cap) S.out_tokens[(size_t)b * S.out_cap + k] = s_tok[j];
+    }
   }
+  // stop after committing the stop token or on reaching the length budget
+  int hit = (j < c && s_tok[j] == S.stop_token && S.stop_token >= 0) ? 1 : 0;
+  hit = __syncthreads_or(hit);
   if (j == 0) {
     S.n_committed[b] = c;
-    S.ncommit_ws[b] = c;
     S.seq_len[b] = L + c;
+    if (S.done && !stopped && (hit || (S.stop_len && L + c >= S.stop_len[b]))) S.done[b] = 1;
   }
 }
 
