@@ -58,7 +58,7 @@ def test_ctypes_struct_layout_matches_c():
     from serving_wedlm_step_gb300 import binding as b
     structs = {"wedlm_config": b.Config, "wedlm_weights": b.Weights,
                "wedlm_slot_rec": b.SlotRec, "wedlm_step_in": b.StepIn,
-               "wedlm_step_out": b.StepOut}
+               "wedlm_step_out": b.StepOut, "wedlm_gen_in": b.GenIn}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', 'int main(void){']
     for cname, py in structs.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')

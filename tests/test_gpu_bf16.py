@@ -10,8 +10,8 @@ import oracle as O
 from synth import (Workload, make_pool_torch, make_state_np, make_weights_torch,
                    qwen3_layers)
 from tests.gpu_common import (Stats, check_pool_writes, compare_seq, dev, pool_bits,
-                              pool_np, run_step, teacher_forced_scores, weights_torch_to_np,
-                              within)
+                              pool_np, resid_bound, run_step, teacher_forced_scores,
+                              weights_torch_to_np, within)
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
@@ -106,13 +106,14 @@ def test_ragged_attention_matches_oracle():
     o_np = o.float().cpu().numpy().reshape(B, W, nq, hd)
     q_np = q.float().cpu().numpy().reshape(B, W, nq, hd)
     pool_f = pool_np(pool)
-    worst = 0.0
+    worst, all_ok = 0.0, True
     for b in range(B):
         kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
         ref = O.window_attention(q_np[b], kp, vp, kw_np[b], vw_np[b])
-        worst = max(worst, float(np.abs(o_np[b] - ref).max()))
+        e, ok = within(o_np[b], ref, TOL, name="attn")
+        worst, all_ok = max(worst, e), all_ok and ok
     print("ragged attention max err", worst)
-    assert worst <= TOL
+    assert all_ok, worst
 
 
 def test_growing_scores_attention_matches_oracle():
@@ -148,13 +149,14 @@ def test_growing_scores_attention_matches_oracle():
     o_np = o.float().cpu().numpy().reshape(B, W, nq, hd)
     q_np = q.float().cpu().numpy().reshape(B, W, nq, hd)
     pool_f = pool_np(pool)
-    worst = 0.0
+    worst, all_ok = 0.0, True
     for b in range(B):
         kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
         ref = O.window_attention(q_np[b], kp, vp, kw_np[b], vw_np[b])
-        worst = max(worst, float(np.abs(o_np[b] - ref).max()))
+        e, ok = within(o_np[b], ref, TOL, name="attn")
+        worst, all_ok = max(worst, e), all_ok and ok
     print("growing-scores attention max err", worst)
-    assert worst <= TOL
+    assert all_ok, worst
 
 
 @pytest.mark.parametrize("B,W,prefix,seed,sample", [
@@ -199,17 +201,22 @@ def test_ragged_layer_matches_oracle(one_layer, B, W, prefix, seed, sample):
         assert np.array_equal(x_in[b * W:(b + 1) * W], emb)
         cos, sin = O.rope_cos_sin(st["pos"][b][p_ref], s.head_dim, s.rope_theta)
         kp, vp = O.pool_gather(pool_f, st["page_table"][b], int(st["seq_len"][b]), s)
+        mid = []
         xr, k, v, o = O.layer_forward(s, w_np["layers"][0], x_in[b * W:(b + 1) * W].astype(np.float64),
-                                      cos, sin, kp, vp, store)
+                                      cos, sin, kp, vp, store, mid=mid)
         wn = win[b].float().cpu().numpy()
         off = O.page_elem_offset(np.arange(W)[:, None], np.arange(s.head_dim)[None, :], s.head_dim)
         kg = np.stack([wn[0, h][off] for h in range(s.n_kv_heads)], 1)
         vg = np.stack([wn[1, h][off] for h in range(s.n_kv_heads)], 1)
         # every tensor here is stored in bf16 by both sides
-        e = {"x": within(x_out[b * W:(b + 1) * W], xr, TOL, True, row_scaled=True, tail=1e-4),
+        # k and v are stored in bf16 by both sides (2e-2 plus two bf16 ulps),
+        # x is the residual stream (resid_bound); the attention output is
+        # held to the flat 2e-2
+        e = {"x": within(x_out[b * W:(b + 1) * W], xr, TOL, name="layer_x",
+                         bound=resid_bound(xr, mid[0], TOL)),
              "attn": within(a_out.float().cpu().numpy()[b * W:(b + 1) * W], o.reshape(W, -1),
-                            TOL, True),
-             "k": within(kg, k, TOL, True), "v": within(vg, v, TOL, True)}
+                            TOL, name="attn"),
+             "k": within(kg, k, TOL, True, name="k"), "v": within(vg, v, TOL, True, name="v")}
         print(b, e)
         for name, (val, ok) in e.items():
             assert ok, (b, name, val)
