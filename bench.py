@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--workload", default="low_entropy",
                     choices=["full_stack", "low_entropy", "one_layer", "ragged", "tiny",
                              "two_layer", "two_layer_long"])
-    ap.add_argument("--extra", default="full_stack,one_layer,ragged,dual_stream",
+    ap.add_argument("--extra", default="full_stack,one_layer,ragged,dual_stream,sweep",
                     help="comma-separated workloads measured after the headline one "
                          "('none' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -111,7 +111,8 @@ def algorithmic_bytes(shape, B, W, prefix_total):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks/throttle reasons sampled every 50 ms (a timed region
+    of 20 steps at ~13 ms is about 260 ms)."""
 
     def __init__(self, index):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -120,7 +121,7 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
@@ -169,30 +170,56 @@ def setup(wl_name, steps, warmup, device, weights=None, loop_steps=0):
     return wl, st, w, pools, plant
 
 
+def _blas_threads():
+    """Threads of the BLAS NumPy loaded: threadpoolctl when installed, else
+    the OpenBLAS library mapped into this process, asked directly."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max(int(i.get("num_threads", 1)) for i in threadpool_info()
+                   if i.get("user_api") == "blas")
+    except Exception:
+        pass
+    import ctypes
+    try:
+        libs = {l.split()[-1] for l in open("/proc/self/maps") if "openblas" in l.lower()}
+    except OSError:
+        libs = set()
+    for path in sorted(libs):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            f = getattr(lib, sym, None)
+            if f is not None:
+                return int(f())
+    return None
+
+
 def host_info():
     """CPU model, core count and the BLAS threads NumPy uses."""
     model = None
     try:
-        for line in open("/proc/cpuinfo"):
-            low = line.lower()
-            if low.startswith("model name") or low.startswith("cpu part") or \
-                    low.startswith("hardware"):
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
                 model = line.split(":", 1)[1].strip()
-                if low.startswith("model name"):
-                    break
-    except OSError:
+                break
+    except Exception:
         pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
     if not model:
         import platform
         model = platform.processor() or platform.machine()
-    blas = None
-    try:
-        from threadpoolctl import threadpool_info
-        blas = max(int(i.get("num_threads", 1)) for i in threadpool_info()
-                   if i.get("user_api") == "blas")
-    except Exception:
-        blas = None
-    return {"cpu": model, "cores": os.cpu_count(), "blas_threads": blas}
+    return {"cpu": model, "cores": os.cpu_count(), "blas_threads": _blas_threads()}
 
 
 def cpu_sample(wl, w, st, ctx_commits_per_step):
@@ -513,6 +540,46 @@ def measure_dual_stream(device, n=4096, block=32, iters=10):
                          "peak_source": f"{src} bf16_tflops (cuBLAS burst)"}}
 
 
+def measure_sweep(device, steps=32, alphas=(0.0, 0.01, 0.05), taus=(1.0, 2.0, 3.0)):
+    """The quality/speed knob of Eq. 11 (Results: the distance penalty "set
+    to balance quality and speed"): for each (alpha, tau), the streaming
+    loop on the device from the same all-masked window over the two-layer
+    low-entropy stack (prefix 32768, W = 32, batch 8, planted counting
+    bias), reporting tokens committed per forward per sequence, slots filled
+    per forward per sequence, and P_c (Key claims §3.1, Eq. 4)."""
+    import torch
+    from serving_wedlm_step_gb300.binding import WedlmContext
+    wl, st, w, pools, plant = setup("two_layer_long", steps, 0, device)
+    s = wl.shape
+    B, W = wl.batch, wl.window
+    ctx = WedlmContext(s, w, window=W, max_batch=B, max_pages_per_seq=st["max_pages"])
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    page_table = T(st["page_table"])
+    plant_t = T(plant)
+    bias = plant_bias_for(s.vocab)
+    out = []
+    for a in alphas:
+        for t in taus:
+            tok, pos, obs = T(st["tokens"]), T(st["pos"]), T(st["obs"])
+            seq_len = T(st["seq_len"])
+            done = torch.zeros(B, dtype=torch.int32, device=device)
+            ran = torch.zeros(1, dtype=torch.int32, device=device)
+            ctx.generate(tok, pos, obs, seq_len, page_table, pools, st["num_pages"], a, t,
+                         steps, done, plant_token=plant_t, plant_bias=bias, steps_run=ran)
+            torch.cuda.synchronize()
+            if ctx.status() != 0:
+                raise RuntimeError("sweep: device error word set")
+            n = int(ran.cpu()[0])
+            committed = int(seq_len.sum()) - int(np.asarray(st["seq_len"]).sum())
+            filled = committed + int(obs.sum()) - int(np.asarray(st["obs"]).sum())
+            out.append({"alpha": a, "tau": t, "steps": n,
+                        "tokens_per_forward": round(committed / (n * B), 3),
+                        "filled_per_forward": round(filled / (n * B), 3),
+                        "prefix_cacheability_Pc": round(committed / (n * B * W), 4)})
+    ctx.close()
+    return {"workload": wl.describe(), "steps_per_point": steps, "points": out}
+
+
 def run_ours(args):
     import torch
     rank, local_rank, world = dist_env()
@@ -550,6 +617,9 @@ def run_ours(args):
         if "dual_stream" in extras_all(args):
             torch.cuda.empty_cache()
             res["extra"]["dual_stream"] = measure_dual_stream(device)
+        if "sweep" in extras_all(args):
+            torch.cuda.empty_cache()
+            res["extra"]["alpha_tau_sweep"] = measure_sweep(device)
     if rank == 0:
         print(json.dumps(res))
 
