@@ -151,9 +151,13 @@ typedef struct wedlm_step_out {
   int32_t *n_committed;        /* [B]                                      */
   int32_t *perm;               /* [B][W] slot at each physical index, or NULL */
   uint8_t *filled;             /* [B][W] 1 where a slot was filled, or NULL */
-  wedlm_slot_rec *rows;        /* [B*W] per PHYSICAL row, or NULL          */
+  wedlm_slot_rec *rows;        /* [B*W] per PHYSICAL row, or NULL.  The LM
+                                  head runs on the masked rows only: an
+                                  observed row's record is argmax -1 and
+                                  NaN statistics                           */
   float *logits;               /* [B*W][vocab] fp32 per physical row, or NULL
-                                  (debug: materialises the logits)         */
+                                  (debug: materialises the logits of the
+                                  masked rows; observed rows are not written) */
   void *hidden;                /* [B*W][hidden] final residual stream, or NULL */
 } wedlm_step_out;
 

@@ -64,7 +64,9 @@ struct wedlm_ctx {
   int* gemm_counters = nullptr;
   int vtiles = 0;
   SoftmaxPart* lm_part = nullptr;
-  wedlm_slot_rec* rows = nullptr;
+  wedlm_slot_rec* rows = nullptr;  // LM-head records, compact (masked rows only)
+  int32_t *lm_src = nullptr, *lm_dst = nullptr, *lm_plant = nullptr;  // MaskedRows
+  int* lm_count = nullptr;
   void* zero_page = nullptr;  // 4 KiB of zeros: stands in for missing KV pages
   // tensor-core GEMM plans (bf16 contexts)
   std::unique_ptr<TcPlanSet> tc;
@@ -267,7 +269,8 @@ GemmProblem gateup_problem(wedlm_ctx* c, int l, int M) {
   P.epi.mode = EPI_SWIGLU; P.epi.act = c->act;
   return P;
 }
-GemmProblem down_problem(wedlm_ctx* c, int l, int M, void* x, const void* next_norm) {
+GemmProblem down_problem(wedlm_ctx* c, int l, int M, void* x, const void* next_norm,
+                         const int32_t* norm_row_dst = nullptr) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
   GemmProblem P{};
@@ -276,6 +279,7 @@ GemmProblem down_problem(wedlm_ctx* c, int l, int M, void* x, const void* next_n
   P.epi.mode = EPI_RESID; P.epi.x = x;
   if (next_norm) {
     P.epi.norm_w = next_norm; P.epi.xn = c->xn; P.epi.eps = g.rms_eps;
+    P.epi.row_dst = norm_row_dst;
   }
   return P;
 }
@@ -299,7 +303,8 @@ template <typename T>
 int layer_impl(wedlm_ctx* c, int l, int B, Win win, T* x, const int32_t* seq_len,
                const int32_t* page_table, int num_pages, const void* pool,
                void* kv_win_layer, cudaStream_t st, bool xn_ready = false,
-               const void* next_norm = nullptr, const Commit& cm = Commit()) {
+               const void* next_norm = nullptr, const Commit& cm = Commit(),
+               const int32_t* norm_row_dst = nullptr) {
   const wedlm_config& g = c->cfg;
   const LayerWeights& w = c->layers[l];
   const int M = B * win.W, H = g.hidden;
@@ -308,7 +313,7 @@ int layer_impl(wedlm_ctx* c, int l, int B, Win win, T* x, const int32_t* seq_len
   GemmProblem Pqkv = qkv_problem(c, l, M, win, kv_win_layer, cm, const_cast<void*>(pool));
   GemmProblem Po = o_problem(c, l, M, x, fuse);
   GemmProblem Pgu = gateup_problem(c, l, M);
-  GemmProblem Pd = down_problem(c, l, M, x, fuse ? next_norm : nullptr);
+  GemmProblem Pd = down_problem(c, l, M, x, fuse ? next_norm : nullptr, norm_row_dst);
   if (!xn_ready)
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, H, x, (const T*)w.attn_norm, g.rms_eps, (T*)c->xn, st));
@@ -329,26 +334,35 @@ int layer_impl(wedlm_ctx* c, int l, int B, Win win, T* x, const int32_t* seq_len
   return WEDLM_OK;
 }
 
-// xn_ready: xn already holds RMSNorm(x) with the final norm
+// xn_ready: xn already holds RMSNorm(x) with the final norm (compacted to
+// the masked rows when mr is set).  mr: the LM head runs on the masked rows
+// only (Method: the scores are needed for the masked slots), compacted in
+// the order mr gives; records, planted tokens and xn rows are compact, the
+// debug logits land on their physical rows.
 template <typename T>
-int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant_phys,
-                float plant_bias, float* logits, cudaStream_t st, bool xn_ready = false) {
+int lmhead_impl(wedlm_ctx* c, int B, const T* x, const int32_t* plant,
+                float plant_bias, float* logits, cudaStream_t st, bool xn_ready = false,
+                const MaskedRows* mr = nullptr) {
   const wedlm_config& g = c->cfg;
   const int M = B * g.window;
   int rc;
   if (!xn_ready)
     LAUNCH(c, WEDLM_KIND_RMSNORM, st,
            launch_rmsnorm<T>(M, g.hidden, x, (const T*)c->final_norm, g.rms_eps,
-                             (T*)c->xn, st));
+                             (T*)c->xn, st, mr ? mr->dst : nullptr));
   GemmProblem P = lmhead_problem(c, M);
   GemmEpi& e = P.epi;
   e.part = c->lm_part; e.mask_id = g.mask_id;
-  e.vocab = g.vocab; e.plant = plant_phys; e.plant_bias = plant_bias;
+  e.vocab = g.vocab; e.plant = mr ? (plant ? mr->plant : nullptr) : plant;
+  e.plant_bias = plant_bias;
   e.logits = logits;
+  e.row_src = mr ? mr->src : nullptr;
+  P.m_count = mr ? mr->count : nullptr;
   int tiles = 0;  // softmax records per row: one per output-feature tile
   if ((rc = run_gemm<T>(c, P, WEDLM_KIND_LMHEAD, st, &tiles))) return rc;
   LAUNCH(c, WEDLM_KIND_LMHEAD_MERGE, st,
-         launch_lmhead_merge(M, tiles, c->lm_part, c->rows, c->err, st));
+         launch_lmhead_merge(M, tiles, c->lm_part, c->rows, c->err, st,
+                             mr ? mr->count : nullptr));
   return WEDLM_OK;
 }
 
@@ -393,16 +407,18 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
   const wedlm_config& g = c->cfg;
   const int B = in->batch, W = g.window, M = B * W;
   int rc;
-  // reorder + embed; also snapshots seq_len and counts the commit run of
-  // every sequence, so the QKV epilogues write the committed K/V to pages
+  // reorder + embed; also snapshots seq_len, counts the commit run of
+  // every sequence (the QKV epilogues write the committed K/V to pages) and
+  // lists the masked rows (the LM head runs on those only)
+  const MaskedRows mr{c->lm_src, c->lm_dst, c->lm_plant, c->lm_count};
   LAUNCH(c, WEDLM_KIND_REORDER, st,
          launch_reorder_embed<T>(B, W, g.hidden, g.head_dim, g.vocab,
                                  g.max_pages_per_seq * kPageBlock, in->tokens,
                                  in->pos, in->observed, in->seq_len,
                                  in->plant_token, (const T*)c->embed, c->inv_freq,
                                  c->perm, c->inv, c->pos_phys, c->seq_snap, c->ncommit,
-                                 x.done, c->plant_phys, (T*)c->x, c->cosb, c->sinb,
-                                 c->err, st));
+                                 x.done, nullptr, (T*)c->x, c->cosb, c->sinb,
+                                 c->err, st, &mr));
   Commit cm;
   cm.n = c->ncommit; cm.base = c->seq_snap; cm.page_table = in->page_table;
   cm.num_pages = in->num_pages;
@@ -413,14 +429,15 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
     void* win = (char*)c->kv_win + (size_t)l * c->win_layer_stride * c->es;
     const void* next_norm =
         !fuse ? nullptr : (l + 1 < g.n_layers ? c->layers[l + 1].attn_norm : c->final_norm);
+    // the last layer's fused final norm writes the masked rows only, compacted
+    const int32_t* row_dst = (fuse && l + 1 == g.n_layers) ? c->lm_dst : nullptr;
     if ((rc = layer_impl<T>(c, l, B, ctx_win(c), (T*)c->x, c->seq_snap, in->page_table,
                             in->num_pages, in->kv_pools[l], win, st, fuse && l > 0,
-                            next_norm, cm)))
+                            next_norm, cm, row_dst)))
       return rc;
   }
-  if ((rc = lmhead_impl<T>(c, B, (const T*)c->x,
-                           in->plant_token ? c->plant_phys : nullptr,
-                           in->plant_bias, out->logits, st, fuse)))
+  if ((rc = lmhead_impl<T>(c, B, (const T*)c->x, in->plant_token, in->plant_bias, out->logits,
+                           st, fuse, &mr)))
     return rc;
   SelArgs S{};
   S.B = B; S.W = W; S.mask_id = g.mask_id; S.alpha = in->alpha; S.tau = in->tau;
@@ -432,12 +449,10 @@ int step_launches(wedlm_ctx* c, const wedlm_step_in* in, wedlm_step_out* out,
   S.new_tokens = out->new_tokens; S.new_pos = out->new_pos;
   S.new_obs = out->new_observed; S.committed = out->committed;
   S.n_committed = out->n_committed; S.ncommit_ws = c->ncommit; S.filled = out->filled;
+  S.row_dst = c->lm_dst; S.out_rows = out->rows;
   LAUNCH(c, WEDLM_KIND_SELECT, st, launch_select(S, st));
   if (out->perm)
     CUDA_TRY(c, cudaMemcpyAsync(out->perm, c->perm, (size_t)M * 4,
-                                cudaMemcpyDeviceToDevice, st));
-  if (out->rows)
-    CUDA_TRY(c, cudaMemcpyAsync(out->rows, c->rows, (size_t)M * sizeof(wedlm_slot_rec),
                                 cudaMemcpyDeviceToDevice, st));
   if (out->hidden)
     CUDA_TRY(c, cudaMemcpyAsync(out->hidden, c->x, (size_t)M * g.hidden * c->es,
@@ -738,6 +753,7 @@ int wedlm_create(const wedlm_config* cfg, const wedlm_weights* w, wedlm_ctx** ou
   WA(C->gemm_counters, (size_t)std::max(C->vtiles, 4096) * 4);
   WA(C->lm_part, (size_t)C->vtiles * M * sizeof(SoftmaxPart));
   WA(C->rows, M * sizeof(wedlm_slot_rec));
+  WA(C->lm_src, M * 4); WA(C->lm_dst, M * 4); WA(C->lm_plant, M * 4); WA(C->lm_count, 256);
   WA(C->zero_page, 4096);
 #undef WA
   if (e != cudaSuccess) {

@@ -137,7 +137,8 @@ __device__ void run_epilogue(const GemmEpi& e, const float* sacc, int m0,
         float zz = sacc[r * 128 + f];
         if (v == pt) zz += e.plant_bias;
         if (v >= e.vocab || v == e.mask_id) zz = -INFINITY;
-        if (e.logits && v < e.vocab) e.logits[(size_t)m * e.vocab + v] = zz;
+        if (e.logits && v < e.vocab)
+          e.logits[(size_t)(e.row_src ? e.row_src[m] : m) * e.vocab + v] = zz;
         z[i] = zz;
         if (zz > mx) { mx = zz; am = v; }
       }
@@ -199,8 +200,9 @@ __device__ void splitk_finish(const GemmProblem& P, float* sacc, int tile) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int m0 = 0; m0 < P.M; m0 += 128) {
-    const int mc = min(128, P.M - m0);
+  const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
+  for (int m0 = 0; m0 < m_live; m0 += 128) {
+    const int mc = min(128, m_live - m0);
     // N is a multiple of 4 and the tile start a multiple of 128, so every
     // float4 lies entirely inside or outside the matrix
 #pragma unroll 4

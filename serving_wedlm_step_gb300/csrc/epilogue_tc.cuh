@@ -216,7 +216,8 @@ __device__ void tc_epilogue_rows(const GemmProblem& P, const AccRow& a, int m, i
         if (z > cm) { cm = z; ca = f; }
       }
       if (e.logits && a.valid && tile * ntile + c < e.vocab) {
-        float* lg = e.logits + (size_t)m * e.vocab + tile * ntile + c;
+        const int lrow = e.row_src ? e.row_src[m] : m;
+        float* lg = e.logits + (size_t)lrow * e.vocab + tile * ntile + c;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (tile * ntile + c + 4 * i < e.vocab)

@@ -109,6 +109,10 @@ struct GemmEpi {
   const int32_t* plant; // [M] or null
   float plant_bias;
   float* logits;        // [M][vocab] or null
+  const int32_t* row_src;  // LMHEAD on compacted rows: logits row of row m, or null
+  // RESID with the next RMSNorm: normed row m goes to row row_dst[m] of xn
+  // (skipped when negative), or to row m when null
+  const int32_t* row_dst;
 };
 
 // One weight-streaming GEMM.  Output features come in tiles of 128 rows of
@@ -123,6 +127,8 @@ struct GemmProblem {
   int seg1, seg2;       // segment row boundaries (QKV); N otherwise
   int swiglu;
   int splits;
+  const int* m_count;   // rows actually present (<= M, read on the device), or
+                        // null for all M; only for splits == 1
   float* partial;       // [splits][M][N] fp32 (splits > 1)
   int* counters;        // [tiles], zero between launches
   int* err;
@@ -155,6 +161,16 @@ struct LayerWeights {
 };
 
 // host launchers (one per kernel family); each returns cudaGetLastError()
+// The masked rows of a step in compact order (LM head on masked slots
+// only): physical row of compact row i, compact row of physical row m (-1
+// for observed rows), the planted token of compact row i, their count.
+struct MaskedRows {
+  int32_t* src;
+  int32_t* dst;
+  int32_t* plant;
+  int* count;
+};
+
 template <typename T>
 cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  int page_cap, const int32_t* tokens,
@@ -165,7 +181,8 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  int32_t* pos_phys, int32_t* seq_snap,
                                  int32_t* ncommit, const int32_t* done,
                                  int32_t* plant_phys, T* x, float* cosb,
-                                 float* sinb, int* err, cudaStream_t st);
+                                 float* sinb, int* err, cudaStream_t st,
+                                 const MaskedRows* mr = nullptr);
 template <typename T>
 cudaError_t launch_prefill_embed(int B, int C, int H, int hd, int vocab, int page_cap,
                                  const int32_t* tokens, const int32_t* seq_len, const T* embed,
@@ -177,9 +194,11 @@ cudaError_t launch_seq_advance(int B, int C, const int32_t* seq_snap, int32_t* s
 cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
                               const double* inv_freq, float* cosb, float* sinb,
                               cudaStream_t st);
+// y[row_dst[m]] = RMSNorm(x[m]) * g (rows with row_dst[m] < 0 skipped), or
+// y[m] when row_dst is null
 template <typename T>
 cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
-                           T* y, cudaStream_t st);
+                           T* y, cudaStream_t st, const int32_t* row_dst = nullptr);
 template <typename T>
 cudaError_t launch_gemm_simt(const GemmProblem& P, cudaStream_t st);
 template <typename T>
@@ -198,7 +217,7 @@ cudaError_t launch_attention_tc(const AttnArgs& A, const void* zero_page, int gr
 int attention_tc_row_blocks(int nq, int nkv, int W, int* rows_per_block);
 cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 wedlm_slot_rec* rows, int* err,
-                                cudaStream_t st);
+                                cudaStream_t st, const int* m_count = nullptr);
 
 enum ScoreMode { SCORE_ENTROPY = 0, SCORE_NEGLOGP = 1 };
 
@@ -230,6 +249,9 @@ struct SelArgs {
   int32_t* n_committed;
   const int32_t* ncommit_ws;  // commit counts found at step start (reorder)
   uint8_t* filled;
+  const int32_t* row_dst;     // compact LM-head row of physical row m, or null
+                              // (records indexed by physical row)
+  wedlm_slot_rec* out_rows;   // [B*W] per physical row (observed: no record), or null
 };
 cudaError_t launch_select(const SelArgs& S, cudaStream_t st);
 

@@ -44,9 +44,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmProblem P) {
   const int arow = tid >> 1, ak = (tid & 1) * 8;
   const T* ap = a_row<T>(P, tile, arow);
   const int xr = tid >> 2, xk = (tid & 3) * 4;
+  // activation rows present (the LM head on masked rows reads their count)
+  const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
 
-  for (int m0 = 0; m0 < P.M; m0 += BNM) {
-    const int mc = min(BNM, P.M - m0);
+  for (int m0 = 0; m0 < m_live; m0 += BNM) {
+    const int mc = min(BNM, m_live - m0);
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmProblem P) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         Xs[(xk + j) * XS_LD + xr] =
-            (m0 + xr < P.M) ? to_f(X[(size_t)(m0 + xr) * P.K + kb * BK + xk + j])
+            (m0 + xr < m_live) ? to_f(X[(size_t)(m0 + xr) * P.K + kb * BK + xk + j])
                             : 0.f;
       __syncthreads();
 #pragma unroll

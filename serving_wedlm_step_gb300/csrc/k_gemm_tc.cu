@@ -96,6 +96,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  // activation rows present (the LM head on masked rows reads their count,
+  // written at the start of the step); row blocks beyond them are skipped
+  const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
+  const int nrb_live = (m_live + 127) / 128;
+  const uint32_t stage_live = (uint32_t)nrb_live * kXBlockBytes + (uint32_t)ntile * 128u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -111,7 +116,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
       auto issue_x = [&](int s, int kx) {
         uint8_t* st = base + (size_t)s * L.stage_bytes;
-        for (int r = 0; r < L.nrb; ++r)
+        for (int r = 0; r < nrb_live; ++r)
           tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
       };
       auto wait_prev = [&]() {
@@ -121,7 +126,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         for (int j = 0; j < npend; ++j) issue_x(pend_s[j], pend_kx[j]);
         npend = 0;
       };
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      for (int u = blockIdx.x; u < units && alive && nrb_live > 0; u += gridDim.x) {
         const int tile = u / P.splits, split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
@@ -136,7 +141,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
           if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
           uint8_t* st = base + (size_t)s * L.stage_bytes;
-          mbar_arrive_expect_tx(&bar_full[s], L.stage_bytes);
+          mbar_arrive_expect_tx(&bar_full[s], stage_live);
           const int kx = kb * kBK;
           // the weight tile in one box (SwiGLU: gate rows, then up rows);
           // rows of 128 bytes one after another, as the MMA descriptors expect
@@ -164,7 +169,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       const uint32_t idesc = idesc_bf16_m128(ntile);
       int it = 0, ul = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++ul) {
+      for (int u = blockIdx.x; u < units && alive && nrb_live > 0; u += gridDim.x, ++ul) {
         const int split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
@@ -181,7 +186,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = sdesc_sw128(sa + L.a_bytes + kk * 32);
-            for (int r = 0; r < L.nrb; ++r) {
+            for (int r = 0; r < nrb_live; ++r) {
               const uint64_t ad = sdesc_sw128(sa + r * kXBlockBytes + kk * 32);
               tc_mma_f16(d0 + (uint32_t)(r * ntile), ad, bd, idesc, (kb != kb0 || kk) ? 1u : 0u);
             }
@@ -197,7 +202,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     pdl_wait();  // outputs and partials may still be read by the previous kernel
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int ul = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
+    for (int u = blockIdx.x; u < units && nrb_live > 0; u += gridDim.x, ++ul) {
       const int tile = u / P.splits, split = u % P.splits;
       const int buf = ul % L.nbuf, use = ul / L.nbuf;
       // on a timeout keep going without waiting (outputs are then invalid and
@@ -205,14 +210,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       // their named barrier
       wait_or_abort(&acc_full[buf], (uint32_t)use & 1u, P.err, &s_abort);
       tc_fence_after();
-      for (int r = 0; r < L.nrb; ++r) {
+      for (int r = 0; r < nrb_live; ++r) {
         const int m = r * 128 + 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols +
                                (uint32_t)(r * ntile);
         if (P.splits == 1) {
-          AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
+          AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < m_live};
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
-        } else if (r * 128 + 32 * q < P.M) {
+        } else if (r * 128 + 32 * q < m_live) {
           // fp32 partial [split][M][N]: the warp's 32 rows x 32 columns go
           // to its staging box in the 128-byte swizzle (16-byte chunk j of
           // row i at chunk j ^ (i % 8): the row-per-lane writes hit every
@@ -335,7 +340,10 @@ __global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmPro
   __syncthreads();
   const float r = rsqrtf(red[0] / (float)P.N + P.epi.eps);
   const bf16* g = static_cast<const bf16*>(P.epi.norm_w);
-  bf16* xn = static_cast<bf16*>(P.epi.xn) + (size_t)m * P.N;
+  // the normed row goes to its compacted row (the LM head on masked rows)
+  const int my = P.epi.row_dst ? P.epi.row_dst[m] : m;
+  if (my < 0) return;  // uniform for the block
+  bf16* xn = static_cast<bf16*>(P.epi.xn) + (size_t)my * P.N;
   for (int i = threadIdx.x; i < n8; i += blockDim.x) {  // this thread's own stores
     Vec16<bf16> v = ld16(x + 8 * i), gv = ld16(g + 8 * i), o;
 #pragma unroll
@@ -636,7 +644,10 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
                            int* tiles_out, int* launches_out) {
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
-  const TcChoice choice = tc_plan(plans, P);
+  TcChoice choice = tc_plan(plans, P);
+  // rows counted on the device (the LM head on masked rows): no split-K, so
+  // that no epilogue kernel has to learn the count
+  if (P.m_count) choice.splits = 1;
   const int ntile = choice.ntile, splits = choice.splits;
   auto tiles_for = [&](int nt) { return tc_tiles_for(P, nt); };
   const int bslot = box_slot(P.swiglu ? ntile / 2 : ntile);
@@ -688,7 +699,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   if (P.splits == 1 && norm) {
     return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
                                 static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
-                                static_cast<bf16*>(P.epi.xn), st);
+                                static_cast<bf16*>(P.epi.xn), st, P.epi.row_dst);
   }
   if (P.splits > 1) {
     const int cap = plans.num_sms * 8;  // grid-stride beyond 8 blocks per SM

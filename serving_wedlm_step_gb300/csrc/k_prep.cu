@@ -33,10 +33,45 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
                      int32_t* perm_ws, int32_t* inv_ws, int32_t* pos_phys,
                      int32_t* seq_snap, int32_t* ncommit,
                      const int32_t* __restrict__ done, int32_t* plant_phys, T* x,
-                     float* cosb, float* sinb, int* err) {
+                     float* cosb, float* sinb, int* err, MaskedRows mr) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   const int p = blockIdx.x, b = blockIdx.y;
+  if (mr.count && p == 0 && b == 0) {
+    // the masked rows of the whole batch in compact order: the masked slots
+    // of sequence bb are its physical rows n_obs..W-1 (Topological
+    // Reordering), in slot order.  The window goes to shared memory, one
+    // thread counts each sequence, one thread scans the counts, and one
+    // thread per sequence writes its rows.
+    const int B = gridDim.y, n = B * W;
+    __shared__ uint8_t s_o[kMaxRows];
+    __shared__ int s_base[kMaxRows + 1];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s_o[i] = obs[i] != 0;
+    __syncthreads();
+    for (int bb = threadIdx.x; bb < B; bb += blockDim.x) {
+      int m = 0;
+      for (int j = 0; j < W; ++j) m += !s_o[bb * W + j];
+      s_base[bb + 1] = m;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_base[0] = 0;
+      for (int bb = 0; bb < B; ++bb) s_base[bb + 1] += s_base[bb];
+      *mr.count = s_base[B];
+    }
+    __syncthreads();
+    for (int bb = threadIdx.x; bb < B; bb += blockDim.x) {
+      const int base = s_base[bb], n_obs = W - (s_base[bb + 1] - base);
+      int k = 0;
+      for (int j = 0; j < W; ++j) {
+        if (s_o[bb * W + j]) continue;
+        mr.src[base + k] = bb * W + n_obs + k;
+        mr.plant[base + k] = plant ? plant[bb * W + j] : -1;
+        ++k;
+      }
+      for (int q = 0; q < W; ++q) mr.dst[bb * W + q] = q < n_obs ? -1 : base + (q - n_obs);
+    }
+  }
   __shared__ int s_slot;
   if (threadIdx.x == 0) {
     // physical index p -> slot: the p-th observed slot, else the
@@ -103,10 +138,13 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  int32_t* perm_ws, int32_t* inv_ws,
                                  int32_t* pos_phys, int32_t* seq_snap, int32_t* ncommit,
                                  const int32_t* done, int32_t* plant_phys, T* x,
-                                 float* cosb, float* sinb, int* err, cudaStream_t st) {
+                                 float* cosb, float* sinb, int* err, cudaStream_t st,
+                                 const MaskedRows* mr) {
+  const MaskedRows none{nullptr, nullptr, nullptr, nullptr};
   return launch_pdl(reorder_embed_kernel<T>, dim3(W, B), dim3(128), 0, st, W, H, hd, vocab,
                     page_cap, tokens, pos, obs, seq_len, plant, embed, inv_freq, perm_ws,
-                    inv_ws, pos_phys, seq_snap, ncommit, done, plant_phys, x, cosb, sinb, err);
+                    inv_ws, pos_phys, seq_snap, ncommit, done, plant_phys, x, cosb, sinb, err,
+                    mr ? *mr : none);
 }
 
 // Prompt prefill rows (all observed, identity order): row p of sequence b
@@ -196,13 +234,15 @@ cudaError_t launch_rope_table(int M, int hd, const int32_t* pos_phys,
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
-               float eps, T* __restrict__ y) {
+               float eps, T* __restrict__ y, const int32_t* __restrict__ row_dst) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   constexpr int N = 16 / sizeof(T);
   const int m = blockIdx.x;
+  const int my = row_dst ? row_dst[m] : m;
+  if (my < 0) return;  // uniform for the block
   const T* xr = x + (size_t)m * H;
-  T* yr = y + (size_t)m * H;
+  T* yr = y + (size_t)my * H;
   const int nv = H / N;
   float ss = 0.f;
   for (int i = threadIdx.x; i < nv; i += blockDim.x) {
@@ -234,8 +274,9 @@ rmsnorm_kernel(int H, const T* __restrict__ x, const T* __restrict__ g,
 
 template <typename T>
 cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
-                           T* y, cudaStream_t st) {
-  return launch_pdl(rmsnorm_kernel<T>, dim3(M), dim3(kNormThreads), 0, st, H, x, g, eps, y);
+                           T* y, cudaStream_t st, const int32_t* row_dst) {
+  return launch_pdl(rmsnorm_kernel<T>, dim3(M), dim3(kNormThreads), 0, st, H, x, g, eps, y,
+                    row_dst);
 }
 
 #define INST(T)                                                               \
@@ -243,9 +284,9 @@ cudaError_t launch_rmsnorm(int M, int H, const T* x, const T* g, float eps,
       int, int, int, int, int, int, const int32_t*, const int32_t*,           \
       const uint8_t*, const int32_t*, const int32_t*, const T*, const double*, \
       int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, const int32_t*,       \
-      int32_t*, T*, float*, float*, int*, cudaStream_t);                      \
+      int32_t*, T*, float*, float*, int*, cudaStream_t, const MaskedRows*);   \
   template cudaError_t launch_rmsnorm<T>(int, int, const T*, const T*, float, \
-                                         T*, cudaStream_t);                   \
+                                         T*, cudaStream_t, const int32_t*);   \
   template cudaError_t launch_prefill_embed<T>(                               \
       int, int, int, int, int, int, const int32_t*, const int32_t*, const T*, \
       const double*, int32_t*, int32_t*, int32_t*, T*, float*, float*, int*,  \

@@ -37,12 +37,12 @@ __device__ __forceinline__ void combine(SoftmaxPart& a, const SoftmaxPart& b) {
 __global__ void lmhead_merge_kernel(int M, int tiles,
                                     const SoftmaxPart* __restrict__ part,
                                     wedlm_slot_rec* __restrict__ rows,
-                                    int* err) {
+                                    int* err, const int* m_count) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= M) return;
+  if (warp >= M || (m_count && warp >= *m_count)) return;
   SoftmaxPart acc;
   acc.m = -INFINITY; acc.a = INT32_MAX; acc.s = 0.f; acc.u = 0.f;
   for (int t = lane; t < tiles; t += 32) combine(acc, part[(size_t)t * M + warp]);
@@ -72,11 +72,11 @@ __global__ void lmhead_merge_kernel(int M, int tiles,
 
 cudaError_t launch_lmhead_merge(int M, int tiles, const SoftmaxPart* part,
                                 wedlm_slot_rec* rows, int* err,
-                                cudaStream_t st) {
+                                cudaStream_t st, const int* m_count) {
   const int threads = 128;
   const int blocks = (M * 32 + threads - 1) / threads;
   return launch_pdl(lmhead_merge_kernel, dim3(blocks), dim3(threads), 0, st, M, tiles, part, rows,
-                    err);
+                    err, m_count);
 }
 
 // ---------------------------------------------------------------------------
@@ -111,8 +111,17 @@ __global__ void __launch_bounds__(kMaxWindow) select_kernel(SelArgs S) {
   }
   __syncthreads();
   const int m0 = s_m0;
+  // a row without a record (observed: the LM head ran on masked rows only)
+  wedlm_slot_rec none;
+  none.argmax = -1;
+  none.entropy = none.p_max = none.lse = __int_as_float(0x7fc00000);
+  auto record = [&](int phys) {  // the record of physical row phys of sequence b
+    const int ci = S.row_dst ? S.row_dst[b * W + phys] : b * W + phys;
+    return ci >= 0 ? S.rows[ci] : none;
+  };
+  if (j < W && S.out_rows) S.out_rows[b * W + j] = record(j);
   if (j < W) {
-    const wedlm_slot_rec rec = S.rows[b * W + S.inv[b * W + j]];
+    const wedlm_slot_rec rec = record(S.inv[b * W + j]);
     s_fill_tok[j] = rec.argmax;
     float ht = __int_as_float(0x7fc00000);  // NaN at observed slots
     int sel = 0;

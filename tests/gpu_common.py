@@ -219,7 +219,8 @@ def _check_decisions(gpu, b, W, ref, scores, st, alpha, tau, stats, mask_id, kin
     obs = st["obs"][b].astype(bool)
     inv = ref.inv
     gaps = top2_gap(scores.logits)
-    for p in range(W):
+    n_obs = int(obs.sum())
+    for p in range(n_obs, W):  # masked rows: the physical suffix
         if gaps[p] < MARGIN:
             stats.excluded_argmax += 1
             continue
@@ -288,9 +289,15 @@ def compare_seq(gpu, b, W, ref: O.SeqStep, st, alpha, tau, tol, stats: Stats,
     assert e2e_scores or tf is not None
     cmp = sc if e2e_scores else tf
     tag = "" if e2e_scores else "_tf"
-    for name, g, r in (("lse", gpu["lse"][rows], cmp.lse),
-                       ("entropy", gpu["entropy"][rows], cmp.entropy),
-                       ("p_max", gpu["p_max"][rows], cmp.p_max)):
+    # the LM head runs on the masked rows only (the physical suffix
+    # n_obs..W-1); observed rows carry no record (argmax -1, NaN)
+    n_obs = int(obs.sum())
+    mrows = slice(b * W + n_obs, (b + 1) * W)
+    assert np.all(gpu["argmax"][b * W:b * W + n_obs] == -1)
+    assert np.all(np.isnan(gpu["entropy"][b * W:b * W + n_obs]))
+    for name, g, r in (("lse", gpu["lse"][mrows], cmp.lse[n_obs:]),
+                       ("entropy", gpu["entropy"][mrows], cmp.entropy[n_obs:]),
+                       ("p_max", gpu["p_max"][mrows], cmp.p_max[n_obs:])):
         e, ok = within(g, r, tol, name=name + tag)
         stats.err(name, e)
         assert ok, f"{name} err {e}"

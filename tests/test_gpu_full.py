@@ -100,7 +100,7 @@ def test_full_stack_step(full):
     # --- LM head records on sampled rows ------------------------------------
     am, H, pm, lse = rows_to_numpy(gpu["rows"])
     hfin = x_chain.float().cpu().numpy().astype(np.float64)
-    sample = [0, 17, 63, 64 + 9, M - 1]
+    sample = [0, 19, 63, 64 + 9, M - 1]  # masked rows (seq 1 and 5: physical rows 0-2 observed)
     hn = store(O.rmsnorm(hfin[sample], w["final_norm"].float().cpu().numpy(), s.rms_eps))
     z = O.lm_head_logits(hn, w["lm_head"].float().cpu().numpy(), s.mask_id)
     sc = O.softmax_scores(z)

@@ -48,10 +48,14 @@ def check_step(s, wl, w_np, st, pools_np, alpha=0.01, tau=1.0, logits=True, grap
         compare_seq(gpu, b, W, ref, st, alpha, tau, TOL, stats, s.mask_id,
                     tf=teacher_forced_scores(gpu, b, W, w_np, s))
         if logits:
-            z = gpu["logits"].numpy()[b * W:(b + 1) * W]
-            fin = np.isfinite(ref.scores.logits)
+            # logits of the masked rows (the physical suffix); observed rows
+            # have none
+            n_obs = int(st["obs"][b].sum())
+            z = gpu["logits"].numpy()[b * W + n_obs:(b + 1) * W]
+            zr = ref.scores.logits[n_obs:]
+            fin = np.isfinite(zr)
             assert np.array_equal(np.isfinite(z), fin)
-            e = np.abs(z[fin] - ref.scores.logits[fin]).max()
+            e = np.abs(z[fin] - zr[fin]).max() if fin.any() else 0.0
             stats.err("logits", e)
             assert e <= TOL
     after = [pool_bits(p) for p in pools]
