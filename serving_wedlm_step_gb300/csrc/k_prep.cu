@@ -8,14 +8,21 @@
 
 namespace wedlm {
 
-// cos/sin of position `p` for pair i: angle p * inv_freq[i] in float64
+// cos/sin of position `p` for pair i.  The angle p * inv_freq[i] is formed
+// in float64 and reduced to [-pi, pi] there (subtracting the nearest
+// multiple of 2 pi; with p < 2^31 and 2 pi held to 2^-53 relative, the
+// reduced angle is good to ~1e-9), then sincosf of the reduced angle: cos
+// and sin are stored in float32, so a float64 sine would be rounded away.
 __device__ __forceinline__ void rope_row(int p, int half, const double* inv_freq,
                                          float* cos_row, float* sin_row) {
+  constexpr double kTwoPi = 6.283185307179586;
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double s, c;
-    sincos((double)p * inv_freq[i], &s, &c);
-    cos_row[i] = (float)c;
-    sin_row[i] = (float)s;
+    const double a = (double)p * inv_freq[i];
+    const double r = fma(-rint(a / kTwoPi), kTwoPi, a);
+    float s, c;
+    sincosf((float)r, &s, &c);
+    cos_row[i] = c;
+    sin_row[i] = s;
   }
 }
 
@@ -37,13 +44,15 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   const int p = blockIdx.x, b = blockIdx.y;
-  if (mr.count && p == 0 && b == 0) {
-    // the masked rows of the whole batch in compact order: the masked slots
-    // of sequence bb are its physical rows n_obs..W-1 (Topological
-    // Reordering), in slot order.  The window goes to shared memory, one
-    // thread counts each sequence, one thread scans the counts, and one
-    // thread per sequence writes its rows.
-    const int B = gridDim.y, n = B * W;
+  if (mr.count && b == (int)gridDim.y - 1) {
+    // an extra row of blocks (b = B) builds the masked-row map beside the
+    // others: the masked rows of the whole batch in compact order (the
+    // masked slots of sequence bb are its physical rows n_obs..W-1 after
+    // Topological Reordering, in slot order).  The window goes to shared
+    // memory, one thread counts each sequence, one thread scans the counts,
+    // and one thread per sequence writes its rows.
+    if (p != 0) return;
+    const int B = gridDim.y - 1, n = B * W;
     __shared__ uint8_t s_o[kMaxRows];
     __shared__ int s_base[kMaxRows + 1];
     for (int i = threadIdx.x; i < n; i += blockDim.x) s_o[i] = obs[i] != 0;
@@ -71,6 +80,7 @@ reorder_embed_kernel(int W, int H, int hd, int vocab, int page_cap,
       }
       for (int q = 0; q < W; ++q) mr.dst[bb * W + q] = q < n_obs ? -1 : base + (q - n_obs);
     }
+    return;
   }
   __shared__ int s_slot;
   if (threadIdx.x == 0) {
@@ -141,7 +151,8 @@ cudaError_t launch_reorder_embed(int B, int W, int H, int hd, int vocab,
                                  float* cosb, float* sinb, int* err, cudaStream_t st,
                                  const MaskedRows* mr) {
   const MaskedRows none{nullptr, nullptr, nullptr, nullptr};
-  return launch_pdl(reorder_embed_kernel<T>, dim3(W, B), dim3(128), 0, st, W, H, hd, vocab,
+  const int rows = B + (mr ? 1 : 0);  // + one row of blocks for the masked-row map
+  return launch_pdl(reorder_embed_kernel<T>, dim3(W, rows), dim3(128), 0, st, W, H, hd, vocab,
                     page_cap, tokens, pos, obs, seq_len, plant, embed, inv_freq, perm_ws,
                     inv_ws, pos_phys, seq_snap, ncommit, done, plant_phys, x, cosb, sinb, err,
                     mr ? *mr : none);
