@@ -1028,6 +1028,7 @@ int wedlm_dual_stream_attention(wedlm_ctx* c, int32_t n, int32_t block, const vo
                          win, o);
   A.max_pages = n_pages;
   A.pt_stride = 0;  // every block reads the one identity row
+  A.kv_reuse = 1;   // and every block re-reads the memory stream's pages
   cudaError_t e;
   {
     Timed t(c, WEDLM_KIND_ATTN, st);

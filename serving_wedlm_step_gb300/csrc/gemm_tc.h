@@ -32,7 +32,8 @@ struct TcChoice {
   int ntile;     // output features per tile
   int splits;    // K splits
 };
-TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P);
+// *t_out (may be null): the modelled time of the plan, seconds
+TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P, double* t_out = nullptr);
 
 // Launches one GEMM; *tiles_out (may be null) receives the number of
 // output-feature tiles (the LM head's softmax records per row) and

@@ -139,6 +139,7 @@ struct AttnArgs {
   int B, W, Wp, nq, nkv, hd, chunk, max_chunks, num_pages, max_pages;
   int pt_stride;        // page-table row of sequence b starts at b * pt_stride
                         // (max_pages; 0: every sequence reads row 0)
+  int kv_reuse;         // 1: pages are read by many units (keep them in L2)
   float scale_log2;     // log2(e) / sqrt(hd)
   const void* q;        // [B*W][nq][hd]
   const void* pool;     // this layer's pool

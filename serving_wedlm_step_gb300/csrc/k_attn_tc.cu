@@ -353,7 +353,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       // ---------------- copiers: K (+ Q) (warp 8), V (warp 10) ----------------
       const int kv = (warp == 10);
       const int NS = kv ? VS : KS;
-      const uint64_t pol = l2_evict_first_policy();
+      // decode reads each cached page once (evict first); Dual-Stream blocks
+      // all re-read the memory stream's pages (keep them)
+      const uint64_t pol = A.kv_reuse ? l2_evict_last_policy() : l2_evict_first_policy();
       const bf16* pool = static_cast<const bf16*>(A.pool);
       const bf16* win = static_cast<const bf16*>(A.kv_win);
       const size_t blockn = (size_t)kPageBlock * hd;

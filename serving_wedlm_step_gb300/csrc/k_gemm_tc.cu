@@ -457,6 +457,239 @@ splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
 }
 
 // ---------------------------------------------------------------------------
+// 2-SM variant for 129..256 activation rows: a cluster of two CTAs (an SM
+// pair) computes one 256-row x (256 * nmma)-feature tile with
+// tcgen05.mma.cta_group::2 (nmma MMAs of N = 256 per K step, one per
+// 256-column accumulator).  CTA r of the pair holds activation rows
+// 128r..128r+127 and, for each MMA, half r of its 256 weight rows in its
+// shared memory, so each SM receives half the tile's activations and half
+// its weights; its TMEM receives its 128 rows of the tile.  Roles as in
+// gemm_tc_kernel:
+//   warp 0 / lane 0 (both CTAs): TMA producer for this CTA's halves; the
+//       loads complete on the even CTA's full barrier (cta_group::2 form),
+//       on which the even CTA's producer set the bytes of both;
+//   warp 1 / lane 0 (even CTA only): MMA issuer; its commits arrive on the
+//       empty / accumulator barriers of both CTAs (multicast);
+//   warps 2-5 (both CTAs): epilogue of this CTA's rows from its own TMEM;
+//       each warp arrives on the even CTA's accumulator-empty barrier.
+// TMEM is allocated and freed by warp 2 of both CTAs together; a cluster
+// barrier after set-up and one before the end keep each CTA's barriers and
+// shared memory alive while the other may use them.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kPairN = 256;                    // N of one pair MMA
+constexpr uint32_t kPairWBytes = 128 * 128;    // one CTA's half of one MMA's weights per stage
+
+template <int NMMA>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
+                    const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mX,
+                    const __grid_constant__ CUtensorMap mPart, GemmProblem P, TcLaunch L) {
+  extern __shared__ uint8_t dsm_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t acc_full[2];
+  __shared__ __align__(8) uint64_t acc_empty[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort, s_issued, s_consumed;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd
+  const int nkb = P.K / kBK;
+  const int units = L.tiles * P.splits;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  constexpr int ntile = NMMA * kPairN, nmma = NMMA;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L.stages; ++s) {
+      mbar_init(&bar_full[s], 1);   // the even CTA's producer (bytes of both CTAs)
+      mbar_init(&bar_empty[s], 1);  // one multicast commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);   // one multicast commit
+      mbar_init(&acc_empty[b], 8);  // the epilogue warps of both CTAs
+    }
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&mW0);
+    tma_prefetch_desc(&mX);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(&s_tmem, L.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  // the even CTA's barriers, as shared::cluster addresses
+  const uint32_t full0 = mapa_shared(smem_u32(&bar_full[0]), 0);
+  const uint32_t accempty0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (this CTA's halves) ----------------
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t stage_all = 2u * L.stage_bytes;  // both CTAs
+      int it = 0;
+      bool alive = true;
+      bool waited = false;
+      int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
+      auto issue_x = [&](int s, int kx) {
+        tma_load_2d_pair_nohint(base + (size_t)s * L.stage_bytes, &mX, full0 + 8u * s, kx,
+                                (int)rank * 128);
+      };
+      auto wait_prev = [&]() {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+        for (int j = 0; j < npend; ++j) issue_x(pend_s[j], pend_kx[j]);
+        npend = 0;
+      };
+      for (int u = pair; u < units && alive; u += npairs) {
+        const int tile = u / P.splits, split = u % P.splits;
+        const int kb0 = (int)((long long)nkb * split / P.splits);
+        const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
+        // this CTA's 128 weight rows of MMA j (D columns 256j..256j+255):
+        // SwiGLU tiles are [gate ntile/2 | up ntile/2], so MMA j < nmma/2
+        // takes gate rows and the rest up rows, 256 features a block; other
+        // tiles take rows tile*ntile + 256j of the q|k|v (or single) weight;
+        // the even CTA the first 128 of each 256, the odd CTA the second
+        const CUtensorMap* segj[NMMA];
+        int rowj[NMMA];
+        for (int j = 0; j < nmma; ++j) {
+          if (P.swiglu) {
+            const int half = nmma / 2;  // MMAs per gate (and up) block
+            const bool up = nmma == 1 ? rank == 1 : j >= half;
+            segj[j] = up ? &mW1 : &mW0;
+            rowj[j] = nmma == 1 ? tile * 128
+                                : tile * (ntile / 2) + (j % half) * kPairN + (int)rank * 128;
+          } else {
+            int r0 = tile * ntile + j * kPairN + (int)rank * 128;
+            const CUtensorMap* sg = &mW0;
+            if (r0 >= P.seg2) { sg = &mW2; r0 -= P.seg2; }
+            else if (r0 >= P.seg1) { sg = &mW1; r0 -= P.seg1; }
+            segj[j] = sg;
+            rowj[j] = r0;
+          }
+        }
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % L.stages;
+          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
+          uint8_t* st = base + (size_t)s * L.stage_bytes;
+          if (rank == 0) mbar_arrive_expect_tx(&bar_full[s], stage_all);
+          const int kx = kb * kBK;
+          for (int j = 0; j < nmma; ++j)
+            tma_load_2d_pair(st + kXBlockBytes + j * kPairWBytes, segj[j], full0 + 8u * s, kx,
+                             rowj[j], pol);
+          if (waited) {
+            issue_x(s, kx);
+          } else {
+            pend_s[npend] = s;
+            pend_kx[npend] = kx;
+            if (++npend == L.stages) wait_prev();
+          }
+        }
+      }
+      if (!waited) wait_prev();
+      s_issued = it;
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
+      // M = 256 over the pair (A: 128 rows in each CTA), N = 256 (B: 128
+      // rows in each CTA)
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                             ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+      int it = 0, ul = 0;
+      bool alive = true;
+      for (int u = pair; u < units && alive; u += npairs, ++ul) {
+        const int split = u % P.splits;
+        const int kb0 = (int)((long long)nkb * split / P.splits);
+        const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
+        const int buf = ul % L.nbuf, use = ul / L.nbuf;
+        if (!wait_or_abort(&acc_empty[buf], ((uint32_t)use & 1u) ^ 1u, P.err, &s_abort)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + (uint32_t)buf * L.buf_cols;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % L.stages;
+          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          if (!wait_or_abort(&bar_full[s], ph, P.err, &s_abort)) { alive = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(base + (size_t)s * L.stage_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            for (int j = 0; j < nmma; ++j)
+              tc_mma_pair_f16(d0 + (uint32_t)(j * kPairN), sdesc_sw128(sa + kk * 32),
+                              sdesc_sw128(sa + kXBlockBytes + j * kPairWBytes + kk * 32), idesc,
+                              (kb != kb0 || kk) ? 1u : 0u);
+          tc_commit_pair(&bar_empty[s], 3);
+        }
+        tc_commit_pair(&acc_full[buf], 3);
+      }
+      s_consumed = it;
+    }
+  } else {
+    // ---------------- epilogue warps: thread = one of this CTA's rows ----------------
+    pdl_wait();  // outputs and partials may still be read by the previous kernel
+    const int q = warp & 3;
+    int ul = 0;
+    for (int u = pair; u < units; u += npairs, ++ul) {
+      const int tile = u / P.splits, split = u % P.splits;
+      const int buf = ul % L.nbuf, use = ul / L.nbuf;
+      wait_or_abort(&acc_full[buf], (uint32_t)use & 1u, P.err, &s_abort);
+      tc_fence_after();
+      const int r = (int)rank;
+      const int m = r * 128 + 32 * q + lane;
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols;
+      if (P.splits == 1) {
+        AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
+        tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
+      } else if (r * 128 + 32 * q < P.M) {
+        const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+        for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c, v);
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_f32x4(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), v[4 * j],
+                            v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&mPart, stg, tile * ntile + c, r * 128 + 32 * q, split);
+            bulk_commit();
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(accempty0 + 8u * buf);  // the even CTA's barrier
+    }
+    if (lane == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (s_abort && threadIdx.x == 0 && rank == 0) {
+    // after a timeout: wait (bounded) for the loads still in flight (both
+    // CTAs' loads complete on the even CTA's full barriers)
+    for (int it = s_consumed; it < s_issued; ++it)
+      mbar_wait(&bar_full[it % L.stages], (uint32_t)(it / L.stages) & 1u, P.err);
+  }
+  __syncthreads();
+  cluster_sync_all();  // the pair is done with each other's barriers and TMEM
+  if (warp == 2) tmem_dealloc_pair(tmem, L.tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -615,7 +848,7 @@ int tc_tiles_for(const GemmProblem& P, int ntile) {
 // The plan of one GEMM: tile width and split-K factor of the persistent
 // kernel (split-K through fp32 partials and an epilogue kernel when
 // splits > 1).
-TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P) {
+TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P, double* t_out) {
   const int nkb = P.K / kBK;
   const int wmax = tc_tile_width(P);
   TcChoice c;
@@ -637,14 +870,177 @@ TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P) {
                                    plans.part_elems, &t);
     if (t < best_t * (1.0 - 1e-9)) { best_t = t; c.ntile = nt; c.splits = s; }
   }
+  if (t_out) *t_out = best_t;
   return c;
+}
+
+cudaError_t launch_gemm_epilogue(const TcPlanSet& plans, const GemmProblem& P, const TcLaunch& L,
+                                 cudaStream_t st);
+
+// The 2-SM pair kernel may take the projections with 129..256 activation
+// rows (two 128-row blocks, one per SM of the pair); the LM head keeps the
+// one-SM kernel (its row count may be known on the device only).
+bool pair_possible(const GemmProblem& P) {
+  if (P.M <= 128 || P.M > 256 || P.epi.mode == EPI_LMHEAD || P.m_count) return false;
+  return P.swiglu ? (P.N / 2) % 128 == 0 : P.N % 128 == 0;
+}
+
+struct PairPlan {
+  int ntile = 0, splits = 1;
+  double t = 1e30;  // modelled seconds
+};
+
+// Pair tile of ntile = 256 or 512 features (one or two N = 256 MMAs per K
+// step) and its split-K factor: units = tiles * s over num_sms/2 pairs,
+// modelled as in tc_choose_splits with each SM receiving its halves of the
+// activations (16 KB) and of every MMA's weights (16 KB each) per 64-wide K
+// block.
+PairPlan pair_plan(const GemmProblem& P, int ntile, int npairs, size_t part_elems) {
+  PairPlan best;
+  if (npairs < 1 || (P.swiglu ? (P.N / 2) % (ntile / 2) : P.N % 128)) return best;
+  const int nmma = ntile / kPairN;
+  const int nkb = P.K / kBK;
+  const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
+  const double per_kb = (double)kXBlockBytes + nmma * (double)kPairWBytes;
+  const double t_all = (double)tiles * nkb * 2.0 * nmma * kPairWBytes / 6.5e12;
+  for (int s = 1; s <= 16; ++s) {
+    if (s > 1 && (nkb / s < 4 || (size_t)s * P.M * P.N > part_elems)) break;
+    const int rounds = (tiles * s + npairs - 1) / npairs;
+    const int kper = (nkb + s - 1) / s;
+    double t = std::max((double)rounds * kper * per_kb / 65e9, t_all);
+    if (s > 1) t += 3e-6 + (double)s * P.M * P.N * 8.0 / 2e12;
+    if (t < best.t * (1.0 - 1e-9)) { best.t = t; best.splits = s; best.ntile = ntile; }
+  }
+  return best;
+}
+
+// How many SM pairs can run the pair kernel at once with `smem` bytes of
+// dynamic shared memory: clusters of two need two SMs of one GPC, so on a
+// chip whose GPCs have odd SM counts this is below SMs / 2.  Asked once per
+// (device, shared-memory size).
+int pair_capacity(size_t smem, int num_sms) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const uint64_t key = ((uint64_t)dev << 32) | (uint64_t)smem;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const void* fn = (const void*)gemm_tc_pair_kernel<1>;  // the same smem and cluster needs as <2>
+  if (ensure_dyn_smem(fn, kMaxDynSmem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  n = std::min(n, num_sms / 2);
+  cache[key] = n;
+  return n;
+}
+
+// dynamic shared memory of a pair launch
+size_t pair_smem(int ntile, int splits) {
+  const uint32_t stage = kXBlockBytes + (uint32_t)(ntile / kPairN) * kPairWBytes;
+  const uint32_t stg = splits > 1 ? 4 * kStageBoxBytes : 0;
+  const uint32_t stages = std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg) / stage);
+  return (size_t)stages * stage + stg + 1024;
+}
+
+cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPlan& pp,
+                             int npairs_max, cudaStream_t st, int* tiles_out, int* launches_out) {
+  const int ntile = pp.ntile, splits = pp.splits, nmma = ntile / kPairN;
+  const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
+  const int bslot = box_slot(128);
+  auto find = [&](const void* w) -> const CUtensorMap* {
+    auto it = plans.maps->weight[bslot].find(w);
+    return it == plans.maps->weight[bslot].end() ? nullptr : &it->second;
+  };
+  const CUtensorMap* a0 = find(P.A0);
+  const CUtensorMap* a1 = find(P.A1);
+  const CUtensorMap* a2 = find(P.A2);
+  if (bslot < 0 || !a0 || !a1 || !a2) return cudaErrorInvalidValue;
+  TcLaunch L;
+  L.ntile = ntile;
+  L.nrb = 1;                                   // one 128-row block per CTA
+  L.buf_cols = ntile;
+  L.nbuf = nmma == 1 ? 2 : 1;                  // 512 TMEM columns either way
+  L.tmem_cols = 512;
+  L.a_bytes = kXBlockBytes;
+  L.stage_bytes = kXBlockBytes + nmma * kPairWBytes;  // 32 or 48 KB: multiples of 1024
+  const uint32_t stg_bytes = splits > 1 ? 4 * kStageBoxBytes : 0;
+  L.stages = (int)std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg_bytes) / L.stage_bytes);
+  L.stg_off = (uint32_t)L.stages * L.stage_bytes;
+  L.tiles = tiles;
+  if (tiles_out) *tiles_out = tiles;
+  P.splits = splits;
+  CUtensorMap mx, mpart;
+  if (!encode_2d(&mx, P.X, P.K, P.M, 128)) return cudaErrorInvalidValue;
+  if (stg_bytes) {
+    if (!P.partial || !encode_partial(&mpart, P.partial, P.N, P.M, splits))
+      return cudaErrorInvalidValue;
+  } else {
+    mpart = mx;  // not read
+  }
+  const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
+  const int units = tiles * splits;
+  const int npairs = std::min(units, npairs_max);
+  const size_t smem = (size_t)L.stages * L.stage_bytes + stg_bytes + 1024;
+  auto kernel = nmma == 1 ? gemm_tc_pair_kernel<1> : gemm_tc_pair_kernel<2>;
+  cudaError_t e = ensure_dyn_smem((const void*)kernel, kMaxDynSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * npairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kernel, *a0, *a1, *a2, mx, mpart, P, L);
+  if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
+  if (e != cudaSuccess) return e;
+  return launch_gemm_epilogue(plans, P, L, st);
 }
 
 cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cudaStream_t st,
                            int* tiles_out, int* launches_out) {
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
-  TcChoice choice = tc_plan(plans, P);
+  double t_one = 0.0;
+  TcChoice choice = tc_plan(plans, P, &t_one);
+  if (pair_possible(P)) {
+    // the pair kernel when its modelled time beats the one-SM plan's, with
+    // as many pairs as can be resident at once (the smallest capacity over
+    // the shared-memory sizes a plan may take)
+    int npairs = plans.num_sms / 2;
+    for (int nt : {256, 512})
+      for (int sp : {1, 2}) npairs = std::min(npairs, pair_capacity(pair_smem(nt, sp), plans.num_sms));
+    PairPlan best;
+    for (int nt : {256, 512}) {
+      const PairPlan pp = pair_plan(P, nt, npairs, plans.part_elems);
+      if (pp.t < best.t) best = pp;
+    }
+    if (best.ntile && best.t < t_one)
+      return launch_gemm_pair(plans, P, best, npairs, st, tiles_out, launches_out);
+  }
   // rows counted on the device (the LM head on masked rows): no split-K, so
   // that no epilogue kernel has to learn the count
   if (P.m_count) choice.splits = 1;
@@ -696,6 +1092,14 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
                               *a2, mx, mpart, P, L);
   if (launches_out) *launches_out = (P.splits > 1 || norm) ? 2 : 1;
   if (le != cudaSuccess) return le;
+  return launch_gemm_epilogue(plans, P, L, st);
+}
+
+// The kernel that follows a GEMM: the RMSNorm of a fused residual without
+// split-K, or the split-K sum with its epilogue.
+cudaError_t launch_gemm_epilogue(const TcPlanSet& plans, const GemmProblem& P, const TcLaunch& L,
+                                 cudaStream_t st) {
+  const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
   if (P.splits == 1 && norm) {
     return launch_rmsnorm<bf16>(P.M, P.N, static_cast<const bf16*>(P.epi.x),
                                 static_cast<const bf16*>(P.epi.norm_w), P.epi.eps,
@@ -718,8 +1122,8 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
       return launch_pdl(splitk_qkv_kernel, dim3((warps + 7) / 8), dim3(256), 0, st, P);
     } else {
       const int items = tc_epi_items(P, L.ntile);
-      return launch_pdl(splitk_epilogue_kernel, dim3(L.tiles * items, L.nrb), dim3(128), 0, st, P,
-                        L.ntile, items);
+      return launch_pdl(splitk_epilogue_kernel, dim3(L.tiles * items, (P.M + 127) / 128),
+                        dim3(128), 0, st, P, L.ntile, items);
     }
   }
   return cudaGetLastError();
