@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="low_entropy",
                     choices=["full_stack", "low_entropy", "one_layer", "ragged", "tiny",
-                             "two_layer", "two_layer_long"])
+                             "two_layer", "two_layer_long", "one_layer_long"])
     ap.add_argument("--extra", default="full_stack,one_layer,ragged,dual_stream,sweep",
                     help="comma-separated workloads measured after the headline one "
                          "('none' for none)")

@@ -139,6 +139,11 @@ WORKLOADS = {
     "two_layer_long": Workload("two_layer_long", qwen3_layers(2), batch=8, window=32,
                                prefix=32768, masked=32, all_masked_start=True,
                                plant=True, steps=256, tau=2.0, seed=0, extra_pages=512),
+    # the low_entropy shapes with 1 layer (about 4 GB on the device), for
+    # full-section profiler captures of single kernels
+    "one_layer_long": Workload("one_layer_long", qwen3_layers(1), batch=8, window=32,
+                               prefix=32768, masked=32, all_masked_start=True,
+                               plant=True, steps=256, tau=2.0, seed=0, extra_pages=512),
     # low-entropy long context: prefix 32768, W=32, batch 8, planted
     # peaked next-token bias on a seeded counting sequence
     "low_entropy": Workload("low_entropy", QWEN3_8B, batch=8, window=32,
