@@ -48,6 +48,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 
 struct TcLaunch {
   int stages, ntile, nrb, nbuf, tiles;
+  int mma_n;         // pair kernel: N of one pair MMA (256, or 192 for SwiGLU tiles of 384)
   uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
   uint32_t stg_off;  // split-K partials: 4 KB staging box per epilogue warp
 };
@@ -219,15 +220,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
         } else if (r * 128 + 32 * q < m_live) {
           // fp32 partial [split][M][N]: the warp's 32 rows x 32 columns go
-          // to its staging box in the 128-byte swizzle (16-byte chunk j of
+          // to a staging box in the 128-byte swizzle (16-byte chunk j of
           // row i at chunk j ^ (i % 8): the row-per-lane writes hit every
           // bank once per 8 lanes) and one lane stores the box with TMA,
-          // whole 128-byte rows; rows and columns outside [M][N] are clipped
-          const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+          // whole 128-byte rows; rows and columns outside [M][N] are clipped.
+          // On the block's last unit the pipeline stages are idle (every
+          // load has landed and every MMA reading them is complete): each
+          // box of the strip gets its own slot there and no store waits for
+          // the one before; otherwise the warp's one staging box is reused.
+          const bool idle = u + (int)gridDim.x >= units && !s_abort &&
+                            (uint32_t)nrb_live * 4u * (uint32_t)(ntile / 32) * kStageBoxBytes <=
+                                (uint32_t)L.stages * L.stage_bytes;
+          const uint32_t slot0 = smem_u32(base) + (uint32_t)((r * 4 + q) * (ntile / 32)) * kStageBoxBytes;
           for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
             float v[32];
             tmem_ld32(taddr + (uint32_t)c, v);
-            if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+            uint32_t stg = slot0 + (uint32_t)(c / 32) * kStageBoxBytes;
+            if (!idle) {
+              stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+              if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+            }
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -458,10 +470,11 @@ splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
 
 // ---------------------------------------------------------------------------
 // 2-SM variant for 129..256 activation rows: a cluster of two CTAs (an SM
-// pair) computes one 256-row x (256 * nmma)-feature tile with
-// tcgen05.mma.cta_group::2 (nmma MMAs of N = 256 per K step, one per
-// 256-column accumulator).  CTA r of the pair holds activation rows
-// 128r..128r+127 and, for each MMA, half r of its 256 weight rows in its
+// pair) computes one 256-row x (mma_n * nmma)-feature tile with
+// tcgen05.mma.cta_group::2 (nmma MMAs of N = mma_n per K step, one per
+// mma_n-column accumulator; mma_n = 256, or 192 for SwiGLU tiles of 192
+// gate + 192 up features).  CTA r of the pair holds activation rows
+// 128r..128r+127 and, for each MMA, half r of its mma_n weight rows in its
 // shared memory, so each SM receives half the tile's activations and half
 // its weights; its TMEM receives its 128 rows of the tile.  Roles as in
 // gemm_tc_kernel:
@@ -476,8 +489,9 @@ splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
 // barrier after set-up and one before the end keep each CTA's barriers and
 // shared memory alive while the other may use them.  Every wait is bounded.
 // ---------------------------------------------------------------------------
-constexpr int kPairN = 256;                    // N of one pair MMA
-constexpr uint32_t kPairWBytes = 128 * 128;    // one CTA's half of one MMA's weights per stage
+constexpr int kPairN = 256;                    // widest N of one pair MMA
+// one CTA's half of one MMA's weights per stage: mma_n / 2 rows x 128 bytes
+__host__ __device__ constexpr uint32_t pair_wbytes(int mma_n) { return (uint32_t)mma_n * 64u; }
 
 template <int NMMA>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -499,7 +513,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
   const int nkb = P.K / kBK;
   const int units = L.tiles * P.splits;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  constexpr int ntile = NMMA * kPairN, nmma = NMMA;
+  constexpr int nmma = NMMA;
+  const int mma_n = L.mma_n, ntile = NMMA * mma_n, hn = mma_n / 2;
+  const uint32_t wbytes = pair_wbytes(mma_n);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
@@ -554,11 +570,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
         const int tile = u / P.splits, split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
-        // this CTA's 128 weight rows of MMA j (D columns 256j..256j+255):
-        // SwiGLU tiles are [gate ntile/2 | up ntile/2], so MMA j < nmma/2
-        // takes gate rows and the rest up rows, 256 features a block; other
-        // tiles take rows tile*ntile + 256j of the q|k|v (or single) weight;
-        // the even CTA the first 128 of each 256, the odd CTA the second
+        // this CTA's mma_n/2 weight rows of MMA j (D columns
+        // mma_n*j..mma_n*(j+1)-1): SwiGLU tiles are [gate ntile/2 | up
+        // ntile/2], so MMA j < nmma/2 takes gate rows and the rest up rows,
+        // mma_n features a block (with one MMA: the even CTA gate, the odd
+        // CTA up rows); other tiles take rows tile*ntile + mma_n*j of the
+        // q|k|v (or single) weight; the even CTA the first half of each
+        // block, the odd CTA the second
         const CUtensorMap* segj[NMMA];
         int rowj[NMMA];
         for (int j = 0; j < nmma; ++j) {
@@ -566,10 +584,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
             const int half = nmma / 2;  // MMAs per gate (and up) block
             const bool up = nmma == 1 ? rank == 1 : j >= half;
             segj[j] = up ? &mW1 : &mW0;
-            rowj[j] = nmma == 1 ? tile * 128
-                                : tile * (ntile / 2) + (j % half) * kPairN + (int)rank * 128;
+            rowj[j] = nmma == 1 ? tile * hn
+                                : tile * (ntile / 2) + (j % half) * mma_n + (int)rank * hn;
           } else {
-            int r0 = tile * ntile + j * kPairN + (int)rank * 128;
+            int r0 = tile * ntile + j * mma_n + (int)rank * hn;
             const CUtensorMap* sg = &mW0;
             if (r0 >= P.seg2) { sg = &mW2; r0 -= P.seg2; }
             else if (r0 >= P.seg1) { sg = &mW1; r0 -= P.seg1; }
@@ -585,7 +603,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
           if (rank == 0) mbar_arrive_expect_tx(&bar_full[s], stage_all);
           const int kx = kb * kBK;
           for (int j = 0; j < nmma; ++j)
-            tma_load_2d_pair(st + kXBlockBytes + j * kPairWBytes, segj[j], full0 + 8u * s, kx,
+            tma_load_2d_pair(st + kXBlockBytes + j * wbytes, segj[j], full0 + 8u * s, kx,
                              rowj[j], pol);
           if (waited) {
             issue_x(s, kx);
@@ -602,10 +620,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (even CTA) ----------------
-      // M = 256 over the pair (A: 128 rows in each CTA), N = 256 (B: 128
-      // rows in each CTA)
+      // M = 256 over the pair (A: 128 rows in each CTA), N = mma_n (B:
+      // mma_n/2 rows in each CTA)
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                             ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+                             ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
       int it = 0, ul = 0;
       bool alive = true;
       for (int u = pair; u < units && alive; u += npairs, ++ul) {
@@ -625,8 +643,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             for (int j = 0; j < nmma; ++j)
-              tc_mma_pair_f16(d0 + (uint32_t)(j * kPairN), sdesc_sw128(sa + kk * 32),
-                              sdesc_sw128(sa + kXBlockBytes + j * kPairWBytes + kk * 32), idesc,
+              tc_mma_pair_f16(d0 + (uint32_t)(j * mma_n), sdesc_sw128(sa + kk * 32),
+                              sdesc_sw128(sa + kXBlockBytes + j * wbytes + kk * 32), idesc,
                               (kb != kb0 || kk) ? 1u : 0u);
           tc_commit_pair(&bar_empty[s], 3);
         }
@@ -651,11 +669,21 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
         AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
         tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
       } else if (r * 128 + 32 * q < P.M) {
-        const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+        // as in gemm_tc_kernel: on the pair's last unit each box of the
+        // warp's strip is staged in its own slot of the idle pipeline stages
+        // (the last MMA, which read both CTAs' stages, is complete)
+        const bool idle = u + npairs >= units && !s_abort &&
+                          4u * (uint32_t)(ntile / 32) * kStageBoxBytes <=
+                              (uint32_t)L.stages * L.stage_bytes;
+        const uint32_t slot0 = smem_u32(base) + (uint32_t)(q * (ntile / 32)) * kStageBoxBytes;
         for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
           float v[32];
           tmem_ld32(taddr + (uint32_t)c, v);
-          if (lane == 0) bulk_wait_read0();
+          uint32_t stg = slot0 + (uint32_t)(c / 32) * kStageBoxBytes;
+          if (!idle) {
+            stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+            if (lane == 0) bulk_wait_read0();
+          }
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -886,30 +914,45 @@ bool pair_possible(const GemmProblem& P) {
 }
 
 struct PairPlan {
-  int ntile = 0, splits = 1;
+  int ntile = 0, mma_n = kPairN, splits = 1;
   double t = 1e30;  // modelled seconds
 };
 
-// Pair tile of ntile = 256 or 512 features (one or two N = 256 MMAs per K
-// step) and its split-K factor: units = tiles * s over num_sms/2 pairs,
-// modelled as in tc_choose_splits with each SM receiving its halves of the
-// activations (16 KB) and of every MMA's weights (16 KB each) per 64-wide K
-// block.
-PairPlan pair_plan(const GemmProblem& P, int ntile, int npairs, size_t part_elems) {
+// Pair tile of ntile = nmma * mma_n features (256 = one N = 256 MMA per K
+// step, 512 = two; 384 = two N = 192 MMAs, SwiGLU only: 192 gate + 192 up
+// features, which puts the Qwen3-8B-sized gate/up projection on 64 tiles
+// instead of 48) and its split-K factor: units = tiles * s over the pairs.
+// Modelled time per K block: each SM receives its halves of the activations
+// (16 KB) and of every MMA's weights (mma_n/2 rows x 128 B), at about
+// 65 GB/s per SM as measured on GB300 inside these kernels, or runs its MMAs
+// (128 cycles per M = 256, N = 256, K = 16 pair MMA), whichever is slower;
+// the whole GPU streams the weights at about 6.5 TB/s at most.  Split-K adds
+// the epilogue launch (about 3 us) and the fp32 partials' round trip, which
+// stays in L2 (s * M * N * 8 bytes at about 4 TB/s: measured at 256 rows,
+// QKV is fastest at 3 splits, O and down at 4).
+PairPlan pair_plan(const GemmProblem& P, int nmma, int mma_n, int npairs, size_t part_elems) {
   PairPlan best;
+  const int ntile = nmma * mma_n;
   if (npairs < 1 || (P.swiglu ? (P.N / 2) % (ntile / 2) : P.N % 128)) return best;
-  const int nmma = ntile / kPairN;
+  if (mma_n != kPairN && !P.swiglu) return best;  // q|k|v segments fall on 128-row halves
   const int nkb = P.K / kBK;
   const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
-  const double per_kb = (double)kXBlockBytes + nmma * (double)kPairWBytes;
-  const double t_all = (double)tiles * nkb * 2.0 * nmma * kPairWBytes / 6.5e12;
+  const double per_kb = std::max(
+      ((double)kXBlockBytes + nmma * (double)pair_wbytes(mma_n)) / 65e9,
+      nmma * (kBK / 16) * 128.0 * mma_n / kPairN / 1.9e9);
+  const double t_all = (double)tiles * nkb * 2.0 * nmma * pair_wbytes(mma_n) / 6.5e12;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && (nkb / s < 4 || (size_t)s * P.M * P.N > part_elems)) break;
     const int rounds = (tiles * s + npairs - 1) / npairs;
     const int kper = (nkb + s - 1) / s;
-    double t = std::max((double)rounds * kper * per_kb / 65e9, t_all);
-    if (s > 1) t += 3e-6 + (double)s * P.M * P.N * 8.0 / 2e12;
-    if (t < best.t * (1.0 - 1e-9)) { best.t = t; best.splits = s; best.ntile = ntile; }
+    double t = std::max((double)rounds * kper * per_kb, t_all);
+    if (s > 1) t += 3e-6 + (double)s * P.M * P.N * 8.0 / 4e12;
+    if (t < best.t * (1.0 - 1e-9)) {
+      best.t = t;
+      best.splits = s;
+      best.ntile = ntile;
+      best.mma_n = mma_n;
+    }
   }
   return best;
 }
@@ -951,8 +994,8 @@ int pair_capacity(size_t smem, int num_sms) {
 }
 
 // dynamic shared memory of a pair launch
-size_t pair_smem(int ntile, int splits) {
-  const uint32_t stage = kXBlockBytes + (uint32_t)(ntile / kPairN) * kPairWBytes;
+size_t pair_smem(int nmma, int mma_n, int splits) {
+  const uint32_t stage = kXBlockBytes + (uint32_t)nmma * pair_wbytes(mma_n);
   const uint32_t stg = splits > 1 ? 4 * kStageBoxBytes : 0;
   const uint32_t stages = std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg) / stage);
   return (size_t)stages * stage + stg + 1024;
@@ -960,9 +1003,9 @@ size_t pair_smem(int ntile, int splits) {
 
 cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPlan& pp,
                              int npairs_max, cudaStream_t st, int* tiles_out, int* launches_out) {
-  const int ntile = pp.ntile, splits = pp.splits, nmma = ntile / kPairN;
+  const int ntile = pp.ntile, splits = pp.splits, mma_n = pp.mma_n, nmma = ntile / mma_n;
   const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
-  const int bslot = box_slot(128);
+  const int bslot = box_slot(mma_n / 2);
   auto find = [&](const void* w) -> const CUtensorMap* {
     auto it = plans.maps->weight[bslot].find(w);
     return it == plans.maps->weight[bslot].end() ? nullptr : &it->second;
@@ -971,14 +1014,16 @@ cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPl
   const CUtensorMap* a1 = find(P.A1);
   const CUtensorMap* a2 = find(P.A2);
   if (bslot < 0 || !a0 || !a1 || !a2) return cudaErrorInvalidValue;
-  TcLaunch L;
+  TcLaunch L{};
   L.ntile = ntile;
+  L.mma_n = mma_n;
   L.nrb = 1;                                   // one 128-row block per CTA
   L.buf_cols = ntile;
   L.nbuf = nmma == 1 ? 2 : 1;                  // 512 TMEM columns either way
   L.tmem_cols = 512;
   L.a_bytes = kXBlockBytes;
-  L.stage_bytes = kXBlockBytes + nmma * kPairWBytes;  // 32 or 48 KB: multiples of 1024
+  // 32, 40 or 48 KB: multiples of 1024, as the 128-byte swizzle wants
+  L.stage_bytes = kXBlockBytes + nmma * pair_wbytes(mma_n);
   const uint32_t stg_bytes = splits > 1 ? 4 * kStageBoxBytes : 0;
   L.stages = (int)std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg_bytes) / L.stage_bytes);
   L.stg_off = (uint32_t)L.stages * L.stage_bytes;
@@ -1030,12 +1075,14 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
     // the pair kernel when its modelled time beats the one-SM plan's, with
     // as many pairs as can be resident at once (the smallest capacity over
     // the shared-memory sizes a plan may take)
+    constexpr int kShapes[3][2] = {{1, 256}, {2, 256}, {2, 192}};  // (nmma, mma_n)
     int npairs = plans.num_sms / 2;
-    for (int nt : {256, 512})
-      for (int sp : {1, 2}) npairs = std::min(npairs, pair_capacity(pair_smem(nt, sp), plans.num_sms));
+    for (const auto& sh : kShapes)
+      for (int sp : {1, 2})
+        npairs = std::min(npairs, pair_capacity(pair_smem(sh[0], sh[1], sp), plans.num_sms));
     PairPlan best;
-    for (int nt : {256, 512}) {
-      const PairPlan pp = pair_plan(P, nt, npairs, plans.part_elems);
+    for (const auto& sh : kShapes) {
+      const PairPlan pp = pair_plan(P, sh[0], sh[1], npairs, plans.part_elems);
       if (pp.t < best.t) best = pp;
     }
     if (best.ntile && best.t < t_one)
@@ -1056,7 +1103,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   const CUtensorMap* a1 = find(P.A1);
   const CUtensorMap* a2 = find(P.A2);
   if (!a0 || !a1 || !a2) return cudaErrorInvalidValue;
-  TcLaunch L;
+  TcLaunch L{};
   L.ntile = ntile;
   L.nrb = (P.M + 127) / 128;
   L.buf_cols = (uint32_t)(L.nrb * L.ntile);
