@@ -305,6 +305,36 @@ def test_streaming_loop_stops_each_sequence():
 # ---------------------------------------------------------------------------
 # the pages' window N = 64 and the confidence score
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,masked,seed", [(8, (36, 60), 2), (5, (8, 40), 3)])
+def test_step_above_256_rows_matches_oracle(B, masked, seed):
+    """More than 256 window rows (B x 64): the LM head on the masked rows
+    takes them in groups of 256 (two row blocks each), only the groups that
+    hold masked rows (B = 8 with 36..60 masked slots of 64: two groups;
+    B = 5 with 8..40: one of two).  The whole step on one Qwen3-8B-shaped
+    layer, 8192-token vocabulary, against the oracle."""
+    s = qwen3_layers(1).replace(vocab=8192)
+    w = make_weights_torch(s, seed=seed, norm_jitter=0.2)
+    w_np = weights_torch_to_np(w)
+    wl = Workload("w64-wide", s, batch=B, window=64, prefix=(100, 400), masked=masked,
+                  shuffled_pages=True, seed=seed)
+    st = make_state_np(wl)
+    pool = make_pool_torch(s, st["num_pages"], seed, 0)
+    ref_pools = [pool_np(pool)]
+    ctx = _ctx(s, w, 64, B, st["max_pages"])
+    gpu = run_step(ctx, st, [pool], st["num_pages"], 0.01, 1.0)
+    assert ctx.status() == 0
+    n_masked = int((st["obs"][:B] == 0).sum())
+    assert n_masked > 256 if B == 8 else n_masked <= 256
+    refs = O.oracle_step(s, w_np, st, ref_pools, 0.01, 1.0)
+    stats = Stats()
+    for b in range(B):
+        tf = teacher_forced_scores(gpu, b, 64, w_np, s)
+        compare_seq(gpu, b, 64, refs[b], st, 0.01, 1.0, TOL, stats, s.mask_id,
+                    bf16_stored=True, tf=tf, e2e_scores=False)
+    print(stats)
+    ctx.close()
+
+
 @pytest.mark.parametrize("B,prefix,seed", [(1, 700, 0), (3, (200, 1500), 1)])
 def test_window_64_step_matches_oracle(B, prefix, seed):
     """A window of 64 slots (the pages' N) at 32 q / 8 kv heads: 256 query
