@@ -48,7 +48,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
 
 struct TcLaunch {
   int stages, ntile, nrb, nbuf, tiles;
-  int mgroups;       // one-SM kernel: row groups of nrb row blocks (LM head above 256 rows)
   int mma_n;         // pair kernel: N of one pair MMA (256, or 192 for SwiGLU tiles of 384)
   uint32_t a_bytes, stage_bytes, tmem_cols, buf_cols;
   uint32_t stg_off;  // split-K partials: 4 KB staging box per epilogue warp
@@ -72,6 +71,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = P.K / kBK;
   const int ntile = L.ntile;
+  const int units = L.tiles * P.splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
@@ -98,18 +98,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   // activation rows present (the LM head on masked rows reads their count,
-  // written at the start of the step); row blocks beyond them are skipped.
-  // The rows are taken in groups of L.nrb row blocks (one group unless the
-  // LM head has more than 256 rows): unit u = (tile, split, group), the
-  // groups of a tile on consecutive units, so blocks running side by side
-  // stream the same weight tile and the second read hits L2; only groups
-  // with live rows are units.
+  // written at the start of the step); row blocks beyond them are skipped
   const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
-  const int rows_grp = L.nrb * 128;
-  const int mg_live = m_live > 0 ? min(L.mgroups, (m_live + rows_grp - 1) / rows_grp) : 0;
-  const int units = L.tiles * P.splits * mg_live;
-  // row blocks of group mg that hold live rows
-  auto nrb_of = [&](int mg) { return min(L.nrb, (m_live - mg * rows_grp + 127) / 128); };
+  const int nrb_live = (m_live + 127) / 128;
+  const uint32_t stage_live = (uint32_t)nrb_live * kXBlockBytes + (uint32_t)ntile * 128u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -122,22 +114,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       // weight boxes goes out before waiting for it, their activation boxes
       // once it is done
       bool waited = false;
-      int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages], pend_mg[kMaxStages];
-      auto issue_x = [&](int s, int kx, int mg) {
+      int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
+      auto issue_x = [&](int s, int kx) {
         uint8_t* st = base + (size_t)s * L.stage_bytes;
-        for (int r = 0; r < nrb_of(mg); ++r)
-          tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, mg * rows_grp + r * 128);
+        for (int r = 0; r < nrb_live; ++r)
+          tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
       };
       auto wait_prev = [&]() {
         pdl_wait();
         pdl_trigger();
         waited = true;
-        for (int j = 0; j < npend; ++j) issue_x(pend_s[j], pend_kx[j], pend_mg[j]);
+        for (int j = 0; j < npend; ++j) issue_x(pend_s[j], pend_kx[j]);
         npend = 0;
       };
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
-        const int mg = u % mg_live, tile = (u / mg_live) / P.splits, split = (u / mg_live) % P.splits;
-        const uint32_t stage_live = (uint32_t)nrb_of(mg) * kXBlockBytes + (uint32_t)ntile * 128u;
+      for (int u = blockIdx.x; u < units && alive && nrb_live > 0; u += gridDim.x) {
+        const int tile = u / P.splits, split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
         const CUtensorMap* seg = &mW0;
@@ -162,11 +153,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
             tma_load_2d_hint(st + L.a_bytes, seg, &bar_full[s], kx, row0, pol);
           }
           if (waited) {
-            issue_x(s, kx, mg);
+            issue_x(s, kx);
           } else {
             pend_s[npend] = s;
             pend_kx[npend] = kx;
-            pend_mg[npend] = mg;
             if (++npend == L.stages) wait_prev();
           }
         }
@@ -180,8 +170,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       const uint32_t idesc = idesc_bf16_m128(ntile);
       int it = 0, ul = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++ul) {
-        const int split = (u / mg_live) % P.splits, nrb_u = nrb_of(u % mg_live);
+      for (int u = blockIdx.x; u < units && alive && nrb_live > 0; u += gridDim.x, ++ul) {
+        const int split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
         const int buf = ul % L.nbuf, use = ul / L.nbuf;
@@ -197,7 +187,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = sdesc_sw128(sa + L.a_bytes + kk * 32);
-            for (int r = 0; r < nrb_u; ++r) {
+            for (int r = 0; r < nrb_live; ++r) {
               const uint64_t ad = sdesc_sw128(sa + r * kXBlockBytes + kk * 32);
               tc_mma_f16(d0 + (uint32_t)(r * ntile), ad, bd, idesc, (kb != kb0 || kk) ? 1u : 0u);
             }
@@ -213,45 +203,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     pdl_wait();  // outputs and partials may still be read by the previous kernel
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     int ul = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++ul) {
-      const int mg = u % mg_live, tile = (u / mg_live) / P.splits, split = (u / mg_live) % P.splits;
-      const int nrb_u = nrb_of(mg);
+    for (int u = blockIdx.x; u < units && nrb_live > 0; u += gridDim.x, ++ul) {
+      const int tile = u / P.splits, split = u % P.splits;
       const int buf = ul % L.nbuf, use = ul / L.nbuf;
       // on a timeout keep going without waiting (outputs are then invalid and
       // the error word says so): the epilogue warps must stay in step at
       // their named barrier
       wait_or_abort(&acc_full[buf], (uint32_t)use & 1u, P.err, &s_abort);
       tc_fence_after();
-      for (int r = 0; r < nrb_u; ++r) {
-        const int rb = mg * L.nrb + r;  // row block within the whole M
-        const int m = rb * 128 + 32 * q + lane;
+      for (int r = 0; r < nrb_live; ++r) {
+        const int m = r * 128 + 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols +
                                (uint32_t)(r * ntile);
         if (P.splits == 1) {
           AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < m_live};
           tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
-        } else if (rb * 128 + 32 * q < m_live) {
+        } else if (r * 128 + 32 * q < m_live) {
           // fp32 partial [split][M][N]: the warp's 32 rows x 32 columns go
-          // to a staging box in the 128-byte swizzle (16-byte chunk j of
+          // to its staging box in the 128-byte swizzle (16-byte chunk j of
           // row i at chunk j ^ (i % 8): the row-per-lane writes hit every
           // bank once per 8 lanes) and one lane stores the box with TMA,
-          // whole 128-byte rows; rows and columns outside [M][N] are clipped.
-          // On the block's last unit the pipeline stages are idle (every
-          // load has landed and every MMA reading them is complete): each
-          // box of the strip gets its own slot there and no store waits for
-          // the one before; otherwise the warp's one staging box is reused.
-          const bool idle = u + (int)gridDim.x >= units && !s_abort &&
-                            (uint32_t)nrb_u * 4u * (uint32_t)(ntile / 32) * kStageBoxBytes <=
-                                (uint32_t)L.stages * L.stage_bytes;
-          const uint32_t slot0 = smem_u32(base) + (uint32_t)((r * 4 + q) * (ntile / 32)) * kStageBoxBytes;
+          // whole 128-byte rows; rows and columns outside [M][N] are clipped
+          const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
           for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
             float v[32];
             tmem_ld32(taddr + (uint32_t)c, v);
-            uint32_t stg = slot0 + (uint32_t)(c / 32) * kStageBoxBytes;
-            if (!idle) {
-              stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
-              if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
-            }
+            if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -260,7 +237,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&mPart, stg, tile * ntile + c, rb * 128 + 32 * q, split);
+              tma_store_3d(&mPart, stg, tile * ntile + c, r * 128 + 32 * q, split);
               bulk_commit();
             }
           }
@@ -1102,19 +1079,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   }
   // rows counted on the device (the LM head on masked rows): no split-K, so
   // that no epilogue kernel has to learn the count
-  // and above 256 rows, groups of two row blocks with the tile width of
-  // 256 rows (fewer, wider tiles than four row blocks would allow; TMEM
-  // holds two 256-column accumulators)
-  int mgroups = 1;
-  if (P.m_count) {
-    choice.splits = 1;
-    if (P.M > 256) {
-      GemmProblem P256 = P;
-      P256.M = 256;
-      choice.ntile = tc_tile_width(P256);
-      mgroups = (P.M + 255) / 256;
-    }
-  }
+  if (P.m_count) choice.splits = 1;
   const int ntile = choice.ntile, splits = choice.splits;
   auto tiles_for = [&](int nt) { return tc_tiles_for(P, nt); };
   const int bslot = box_slot(P.swiglu ? ntile / 2 : ntile);
@@ -1129,8 +1094,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   if (!a0 || !a1 || !a2) return cudaErrorInvalidValue;
   TcLaunch L{};
   L.ntile = ntile;
-  L.mgroups = mgroups;
-  L.nrb = mgroups > 1 ? 2 : (P.M + 127) / 128;
+  L.nrb = (P.M + 127) / 128;
   L.buf_cols = (uint32_t)(L.nrb * L.ntile);
   L.nbuf = L.buf_cols * 2 <= 512 ? 2 : 1;
   L.a_bytes = (uint32_t)L.nrb * kXBlockBytes;
@@ -1156,7 +1120,7 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
   L.tiles = tiles_for(ntile);
   if (tiles_out) *tiles_out = L.tiles;
   P.splits = splits;
-  const int units = L.tiles * P.splits * mgroups;
+  const int units = L.tiles * P.splits;
   const bool norm = P.epi.mode == EPI_RESID && P.epi.norm_w;
   const int grid = std::min(units, plans.num_sms);
   const size_t smem = (size_t)L.stages * L.stage_bytes + stg_bytes + 1024;

@@ -308,10 +308,11 @@ def test_streaming_loop_stops_each_sequence():
 @pytest.mark.parametrize("B,masked,seed", [(8, (36, 60), 2), (5, (8, 40), 3)])
 def test_step_above_256_rows_matches_oracle(B, masked, seed):
     """More than 256 window rows (B x 64): the LM head on the masked rows
-    takes them in groups of 256 (two row blocks each), only the groups that
-    hold masked rows (B = 8 with 36..60 masked slots of 64: two groups;
-    B = 5 with 8..40: one of two).  The whole step on one Qwen3-8B-shaped
-    layer, 8192-token vocabulary, against the oracle."""
+    runs with 128-wide vocabulary tiles and up to four row blocks, of which
+    only those holding masked rows are loaded and multiplied (B = 8 with
+    36..60 masked slots of 64: more than 256 rows; B = 5 with 8..40: at
+    most 200 of 320).  The whole step on one Qwen3-8B-shaped layer,
+    8192-token vocabulary, against the oracle."""
     s = qwen3_layers(1).replace(vocab=8192)
     w = make_weights_torch(s, seed=seed, norm_jitter=0.2)
     w_np = weights_torch_to_np(w)
