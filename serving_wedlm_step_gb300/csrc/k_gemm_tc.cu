@@ -540,7 +540,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
       // ---------------- TMA producer (this CTA's halves) ----------------
       const uint64_t pol = l2_evict_first_policy();
       const uint32_t stage_all = 2u * L.stage_bytes;  // both CTAs
-      int it = 0;
+      int it = 0, ps = 0;
+      uint32_t pph = 0;
       bool alive = true;
       bool waited = false;
       int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
@@ -585,8 +586,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
           }
         }
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % L.stages;
-          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          const int s = ps;
+          const uint32_t ph = pph;
+          if (++ps == L.stages) {  // the ring position of the next K block
+            ps = 0;
+            pph ^= 1u;
+          }
           if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
           uint8_t* st = base + (size_t)s * L.stage_bytes;
           if (rank == 0) mbar_arrive_expect_tx(&bar_full[s], stage_all);
@@ -613,7 +618,16 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
       // mma_n/2 rows in each CTA)
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
                              ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
-      int it = 0, ul = 0;
+      // This one thread feeds the tensor pipe, so its per-K-block scalar
+      // work is kept small: the ring stage and phase advance by one step
+      // (no division), the operand descriptors are formed once per stage
+      // and stepped along K by adding the 32-byte offset (2 in the
+      // descriptor's 16-byte address units).
+      const uint64_t da0 = sdesc_sw128(smem_u32(base));
+      const uint64_t dstage = (uint64_t)(L.stage_bytes >> 4);
+      const uint64_t dw = (uint64_t)(wbytes >> 4), dx = (uint64_t)(kXBlockBytes >> 4);
+      int it = 0, ul = 0, s = 0;
+      uint32_t ph = 0;
       bool alive = true;
       for (int u = pair; u < units && alive; u += npairs, ++ul) {
         const int split = u % P.splits;
@@ -624,18 +638,21 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)buf * L.buf_cols;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % L.stages;
-          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
           if (!wait_or_abort(&bar_full[s], ph, P.err, &s_abort)) { alive = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(base + (size_t)s * L.stage_bytes);
+          const uint64_t da = da0 + (uint64_t)s * dstage;  // this stage's activation block
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
+#pragma unroll
             for (int j = 0; j < nmma; ++j)
-              tc_mma_pair_f16(d0 + (uint32_t)(j * mma_n), sdesc_sw128(sa + kk * 32),
-                              sdesc_sw128(sa + kXBlockBytes + j * wbytes + kk * 32), idesc,
+              tc_mma_pair_f16(d0 + (uint32_t)(j * mma_n), da + (uint64_t)(2 * kk),
+                              da + dx + (uint64_t)j * dw + (uint64_t)(2 * kk), idesc,
                               (kb != kb0 || kk) ? 1u : 0u);
           tc_commit_pair(&bar_empty[s], 3);
+          if (++s == L.stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         tc_commit_pair(&acc_full[buf], 3);
       }
