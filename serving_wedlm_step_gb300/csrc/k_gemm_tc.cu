@@ -108,7 +108,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       // ---------------- TMA producer ----------------
       const uint64_t pol = l2_evict_first_policy();
       const int half = ntile / 2;
-      int it = 0;
+      int it = 0, ps = 0;
+      uint32_t pph = 0;
       bool alive = true;
       // weights do not depend on the previous kernel: the first ring of
       // weight boxes goes out before waiting for it, their activation boxes
@@ -138,8 +139,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
           else if (row0 >= P.seg1) { seg = &mW1; row0 -= P.seg1; }
         }
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % L.stages;
-          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
+          const int s = ps;
+          const uint32_t ph = pph;
+          if (++ps == L.stages) {  // the ring position of the next K block
+            ps = 0;
+            pph ^= 1u;
+          }
           if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
           uint8_t* st = base + (size_t)s * L.stage_bytes;
           mbar_arrive_expect_tx(&bar_full[s], stage_live);
@@ -168,7 +173,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       const uint32_t idesc = idesc_bf16_m128(ntile);
-      int it = 0, ul = 0;
+      // as in the pair kernel: stage and phase stepped, descriptors formed
+      // once per stage and stepped along K (2 = 32 bytes in 16-byte units)
+      const uint64_t da0 = sdesc_sw128(smem_u32(base));
+      const uint64_t dstage = (uint64_t)(L.stage_bytes >> 4), dw = (uint64_t)(L.a_bytes >> 4);
+      const uint64_t dx = (uint64_t)(kXBlockBytes >> 4);
+      int it = 0, ul = 0, s = 0;
+      uint32_t ph = 0;
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive && nrb_live > 0; u += gridDim.x, ++ul) {
         const int split = u % P.splits;
@@ -179,20 +190,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)buf * L.buf_cols;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % L.stages;
-          const uint32_t ph = (uint32_t)(it / L.stages) & 1u;
           if (!wait_or_abort(&bar_full[s], ph, P.err, &s_abort)) { alive = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(base + (size_t)s * L.stage_bytes);
+          const uint64_t da = da0 + (uint64_t)s * dstage;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(sa + L.a_bytes + kk * 32);
-            for (int r = 0; r < nrb_live; ++r) {
-              const uint64_t ad = sdesc_sw128(sa + r * kXBlockBytes + kk * 32);
-              tc_mma_f16(d0 + (uint32_t)(r * ntile), ad, bd, idesc, (kb != kb0 || kk) ? 1u : 0u);
-            }
+            const uint64_t bd = da + dw + (uint64_t)(2 * kk);
+            for (int r = 0; r < nrb_live; ++r)
+              tc_mma_f16(d0 + (uint32_t)(r * ntile), da + (uint64_t)r * dx + (uint64_t)(2 * kk), bd,
+                         idesc, (kb != kb0 || kk) ? 1u : 0u);
           }
           tc_commit(&bar_empty[s]);
+          if (++s == L.stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         tc_commit(&acc_full[buf]);
       }
