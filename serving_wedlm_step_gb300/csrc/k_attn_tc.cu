@@ -391,6 +391,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
         return true;
       };
       int seg = -1;
+      int cst = 0;        // ring stage of tile i (i % NS, stepped)
+      uint32_t cph = 0;   // and its phase ((i / NS) & 1)
       Cur cur = first;
       for (int i = 0; i < ntiles; ++i, advance(cur)) {
         const int b = cur.b, kvh = cur.kvh, t = cur.t;
@@ -426,8 +428,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
             pid[pg] = v;
           }
         }
-        const int st = i % NS;
-        const uint32_t ph = (uint32_t)(i / NS) & 1u;
+        const int st = cst;
+        const uint32_t ph = cph;
+        if (++cst == NS) {
+          cst = 0;
+          cph ^= 1u;
+        }
         uint64_t* full = kv ? &v_full[st] : &k_full[st];
         if (!wait(kv ? &v_empty[st] : &k_empty[st], ph ^ 1u)) break;
         uint8_t* dst = base + (kv ? Ly.off_v : Ly.off_k) + st * kKVBytes;
@@ -461,6 +467,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       const uint64_t dk0 = sdesc_noswz(smem_u32(base + Ly.off_k), 128, 2048);
       const uint64_t dq_step = (uint64_t)((2 * qlbo) >> 4);  // 16 dims, in 16-byte units
       int seg = -1;
+      int kst = 0, sbi = 0;       // K stage (i % KS) and S buffer (i % 3), stepped
+      uint32_t kph = 0, sph = 0;  // their phases
       Cur cs = first;
       for (int i = 0; i < ntiles; ++i, advance(cs)) {
         const int t = cs.t, T = cs.T;
@@ -471,11 +479,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
           if (!wait(&q_full[seg & 1], (uint32_t)(seg >> 1) & 1u)) break;
           s_done[2] = seg + 1;
         }
-        const int st = i % KS, sb = i % kSBuf;
-        if (!wait(&k_full[st], (uint32_t)(i / KS) & 1u)) break;
+        const int st = kst, sb = sbi;
+        const uint32_t kp = kph, spp = sph;
+        if (++kst == KS) {
+          kst = 0;
+          kph ^= 1u;
+        }
+        if (++sbi == kSBuf) {
+          sbi = 0;
+          sph ^= 1u;
+        }
+        if (!wait(&k_full[st], kp)) break;
         s_done[0] = i + 1;
         // S buffer sb is free once P V of tile i - 3 is done
-        if (!wait(&s_free[sb], ((uint32_t)(i / kSBuf) & 1u) ^ 1u)) break;
+        if (!wait(&s_free[sb], spp ^ 1u)) break;
         tc_fence_after();
         const uint64_t aq = (seg & 1) ? dq1 : dq0;
         const uint64_t bk = dk0 + (uint64_t)((st * kKVBytes) >> 4);
@@ -495,14 +512,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
       const uint32_t idPV = idesc_pv();
       const uint64_t dv0 = sdesc_noswz(smem_u32(base + Ly.off_v), 2048, 128);
       int seg = -1;
+      int vst = 0, pbi = 0;       // V stage (i % VS) and P buffer (i % 3), stepped
+      uint32_t vph = 0, pph = 0;  // their phases
       Cur cp = first;
       for (int i = 0; i < ntiles; ++i, advance(cp)) {
         const int t = cp.t;
         const bool seg_first = (i == 0 || t == 0);
-        const int st = i % VS, pb = i % kSBuf;
-        if (!wait(&v_full[st], (uint32_t)(i / VS) & 1u)) break;
+        const int st = vst, pb = pbi;
+        const uint32_t vp = vph, pp = pph;
+        if (++vst == VS) {
+          vst = 0;
+          vph ^= 1u;
+        }
+        if (++pbi == kSBuf) {
+          pbi = 0;
+          pph ^= 1u;
+        }
+        if (!wait(&v_full[st], vp)) break;
         s_done[1] = i + 1;
-        if (!wait(&p_full[pb], (uint32_t)(i / kSBuf) & 1u)) break;
+        if (!wait(&p_full[pb], pp)) break;
         if (seg_first) {
           // O is overwritten: the previous segment's O must have been read
           ++seg;
