@@ -282,6 +282,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   const uint32_t tmem = s_tmem;
   volatile int* abort = &s_abort;
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;  // completed: one poll, no flag read
     if (*abort) return false;
     if (mbar_wait(bar, parity, A.err)) return true;
     *abort = 1;

@@ -39,6 +39,9 @@ constexpr int kMaxDynSmem = 221 * 1024;
 // bounded wait that gives up at once after any wait of this block timed out
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* err,
                                               volatile int* abort) {
+  // a phase that has already completed costs one poll (the issuing threads
+  // are on the critical path); the abort flag is read only when waiting
+  if (mbar_try_wait(bar, parity)) return true;
   if (*abort) return false;
   if (mbar_wait(bar, parity, err)) return true;
   *abort = 1;
