@@ -223,6 +223,7 @@ AttnArgs attn_args(wedlm_ctx* c, int B, Win win, const void* q, const void* pool
   A.kv_win = kv_win; A.part_o = c->attn_o; A.part_ml = c->attn_ml; A.o = o;
   A.err = c->err;
   A.min_tiles = 2;
+  A.unit_cost = kAttnUnitCost;
   A.unit_cnt = c->attn_unit_cnt;
   return A;
 }

@@ -135,6 +135,12 @@ struct GemmProblem {
   GemmEpi epi;
 };
 
+// A tensor-core attention unit's start (Q, the first tile) and end (normalise
+// and write, or partial and merge) cost about as much as this many of its
+// 128-key tiles; the stream-K shares count them (measured on Dual-Stream
+// blocks, whose units are short).
+constexpr int kAttnUnitCost = 4;
+
 struct AttnArgs {
   int B, W, Wp, nq, nkv, hd, chunk, max_chunks, num_pages, max_pages;
   int pt_stride;        // page-table row of sequence b starts at b * pt_stride
@@ -152,6 +158,9 @@ struct AttnArgs {
   int* err;
   // tensor-core (stream-K) attention: partials per segment
   int min_tiles;        // fewest 64-key tiles a block is given
+  int unit_cost;        // tensor-core attention: tiles' worth of time a unit's
+                        // start and end cost, counted when the work is cut
+                        // into the blocks' shares (0: tiles only)
   int* unit_cnt;        // [B*nkv]: segments of each unit written so far (zero
                         // between launches; the unit's merging block resets it)
 };

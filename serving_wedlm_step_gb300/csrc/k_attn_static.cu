@@ -98,6 +98,7 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
   A.kv_win = kv_win; A.part_o = part_o; A.part_ml = part_ml; A.o = o;
   A.err = reinterpret_cast<int*>(scratch + kErrOff);
   A.min_tiles = 2;
+  A.unit_cost = kAttnUnitCost;  // the same split as wedlm_attention
   A.unit_cnt = unit_cnt;
   if (launch_attention_tc(A, scratch + kZeroOff, sms, st) != cudaSuccess) return WEDLM_ERR_CUDA;
   return WEDLM_OK;

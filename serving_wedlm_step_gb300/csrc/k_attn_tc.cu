@@ -97,11 +97,15 @@ struct AttnLayout {
 };
 
 // Split of the flattened tile sequence over the blocks; every block and the
-// segment table agree on it.
+// segment table agree on it.  The shares are equal in weighted length: a
+// unit weighs its tiles plus unit_cost, the time its start (Q, first tile)
+// and end (normalise and write, or partial and merge) take, so that a block
+// of many short units gets fewer tiles.
 struct StreamSplit {
-  long long total;  // tiles of all units
-  int G;            // blocks that get work
-  __device__ long long begin(int c) const { return (long long)c * total / G; }
+  long long total;    // tiles of all units
+  long long total_w;  // their weighted length
+  int G;              // blocks that get work
+  __device__ long long begin_w(int c) const { return (long long)c * total_w / G; }
 };
 
 // largest index i in [0, n) with a[i] <= x (a ascending, a[0] <= x)
@@ -208,7 +212,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   __shared__ long long s_tstart[kMaxB + 1];    // first global tile of sequence b
   __shared__ long long s_begin[kMaxGrid + 1];  // first global tile of block c
   __shared__ int s_P[kMaxB];                   // prefix tiles of sequence b
-  __shared__ int s_pages[kPrefTiles * kPagesPerTile];  // page ids (-1: none)
+  // page ids (-1: none); before they are loaded, the same bytes hold the
+  // first weighted position of each sequence (the plan's split)
+  __shared__ __align__(8) int s_pages[kPrefTiles * kPagesPerTile];
+  static_assert(sizeof(int) * kPrefTiles * kPagesPerTile >= sizeof(long long) * (kMaxB + 1),
+                "the weighted starts must fit the page-id table");
+  long long* s_wstart = reinterpret_cast<long long*>(s_pages);
   __shared__ StreamSplit s_split;
 
   const int hd = 128, G = A.nq / A.nkv, W = A.W, R = Ly.R;
@@ -226,29 +235,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   // segment to the next, so slots are distinct and fewer than units + G.
   for (int b = threadIdx.x; b < A.B; b += kThreads) s_P[b] = prefix_tiles(A, b);
   __syncthreads();
+  const int ucost = max(0, A.unit_cost);
+  // weighted length of the units of one kv head of a sequence with P prefix tiles
+  auto head_weight = [&](int P) { return (long long)NRB * (P + ucost) + Ly.cwt[NRB]; };
   if (warp == 0) {
     const int per = (A.B + 31) / 32;
     const int b0 = min(A.B, lane * per), b1 = min(A.B, b0 + per);
-    long long sum = 0;
-    for (int b = b0; b < b1; ++b) sum += (long long)head_tiles(s_P[b]) * A.nkv;
-    long long incl = sum;
+    long long sum = 0, sumw = 0;
+    for (int b = b0; b < b1; ++b) {
+      sum += (long long)head_tiles(s_P[b]) * A.nkv;
+      sumw += head_weight(s_P[b]) * A.nkv;
+    }
+    long long incl = sum, inclw = sumw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
+      const long long xw = __shfl_up_sync(0xffffffffu, inclw, o);
+      if (lane >= o) {
+        incl += x;
+        inclw += xw;
+      }
     }
-    long long acc = incl - sum;
+    long long acc = incl - sum, accw = inclw - sumw;
     for (int b = b0; b < b1; ++b) {
       s_tstart[b] = acc;
+      s_wstart[b] = accw;
       acc += (long long)head_tiles(s_P[b]) * A.nkv;
+      accw += head_weight(s_P[b]) * A.nkv;
     }
     if (lane == 31) {
       StreamSplit sp;
       sp.total = incl;
+      sp.total_w = inclw;
       const long long by_min = (incl + A.min_tiles - 1) / A.min_tiles;
       sp.G = (int)min((long long)min((int)gridDim.x, kMaxGrid), max(1LL, by_min));
       s_split = sp;
       s_tstart[A.B] = incl;
+      s_wstart[A.B] = inclw;
     }
   }
   if (threadIdx.x == 32) {
@@ -270,7 +293,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mq, AttnArgs A, AttnLayout Ly
   __syncthreads();
   const StreamSplit sp = s_split;
   if ((int)blockIdx.x >= sp.G) return;  // uniform for the block
-  for (int c = threadIdx.x; c <= sp.G; c += kThreads) s_begin[c] = sp.begin(c);
+  // first tile of each block: its weighted start mapped to the tile it
+  // falls on (a start inside a unit's cost lands on the unit's first tile,
+  // so a block may be given no tiles, only ever at a unit's start)
+  for (int c = threadIdx.x; c <= sp.G; c += kThreads) {
+    const long long w = sp.begin_w(c);
+    long long g = sp.total;
+    if (w < sp.total_w) {
+      const int b = last_le(s_wstart, A.B, w);
+      const int P = s_P[b];
+      const long long off = w - s_wstart[b], H = head_weight(P);
+      const int kvh = (int)(off / H);
+      const long long r = off % H;
+      int rb = 0;
+      while (rb + 1 < NRB && (long long)(rb + 1) * (P + ucost) + Ly.cwt[rb + 1] <= r) ++rb;
+      const long long x = r - ((long long)rb * (P + ucost) + Ly.cwt[rb]);
+      const long long t = max(0LL, x - ucost);  // < P + wt[rb]
+      g = s_tstart[b] + (long long)kvh * head_tiles(P) + (long long)rb * P + Ly.cwt[rb] + t;
+    }
+    s_begin[c] = g;
+  }
   __syncthreads();
   if (warp == 0) {
     tmem_alloc(&s_tmem, kTmemCols);
