@@ -1031,8 +1031,8 @@ int wedlm_dual_stream_attention(wedlm_ctx* c, int32_t n, int32_t block, const vo
   A.pt_stride = 0;  // every block reads the one identity row
   A.kv_reuse = 1;   // and every block re-reads the memory stream's pages
   // units here are short (a block and its prefix): counting their start and
-  // end as eight tiles balances the shares best (measured at n = 4096, blocks
-  // of 32: 0.445 ms against 0.472 ms with four)
+  // end as six tiles balances the shares best (measured at n = 4096, blocks
+  // of 32: 0.437 ms, against 0.445 ms with eight and 0.472 ms with four)
   A.unit_cost = 2 * kAttnUnitCost;
   cudaError_t e;
   {

@@ -137,9 +137,9 @@ struct GemmProblem {
 
 // A tensor-core attention unit's start (Q, the first tile) and end (normalise
 // and write, or partial and merge) cost about as much as this many of its
-// 128-key tiles; the stream-K shares count them (measured on Dual-Stream
-// blocks, whose units are short).
-constexpr int kAttnUnitCost = 4;
+// 128-key tiles; the stream-K shares count them.  Swept 0..8 on GB300: 3 is
+// best for the decode step (0 is the plain tile split).
+constexpr int kAttnUnitCost = 3;
 
 struct AttnArgs {
   int B, W, Wp, nq, nkv, hd, chunk, max_chunks, num_pages, max_pages;
