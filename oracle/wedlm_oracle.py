@@ -245,13 +245,23 @@ def dual_stream_visibility(n, block):
     before the block, 0..j*block-1, and the keys of its own block at physical
     index <= p (causal in the reordered order)."""
     vis = np.zeros((2 * n, 2 * n), bool)
-    for r in range(n):
-        vis[r, :r + 1] = True
-    for i in range(n):
-        j, p = divmod(i, block)
-        vis[n + i, :j * block] = True
-        vis[n + i, n + j * block:n + j * block + p + 1] = True
+    for r in range(2 * n):
+        vis[r] = dual_stream_visible_row(n, block, r)
     return vis
+
+
+def dual_stream_visible_row(n, block, r):
+    """Row r of the Dual-Stream visibility above (same rule, one query row):
+    a memory row sees the memory up to itself, a prediction row the memory
+    before its block and its own block causally."""
+    v = np.zeros(2 * n, bool)
+    if r < n:
+        v[:r + 1] = True
+    else:
+        j, p = divmod(r - n, block)
+        v[:j * block] = True
+        v[n + j * block:n + j * block + p + 1] = True
+    return v
 
 
 def dual_stream_attention(q, k_mem, v_mem, k_pred, v_pred, block):
@@ -277,6 +287,28 @@ def dual_stream_attention(q, k_mem, v_mem, k_pred, v_pred, block):
         p = np.exp(s)
         p = p / p.sum(axis=1, keepdims=True)
         out[:, h] = p @ vals[:, g]
+    return out
+
+
+def dual_stream_attention_rows(q, k_mem, v_mem, k_pred, v_pred, block, rows):
+    """dual_stream_attention for the query rows `rows` only (indices into the
+    2n rows; q holds all 2n): the same softmax over each row's visible keys,
+    for checking sampled rows of a call too large to evaluate whole.
+    Returns [len(rows)][nq][hd]."""
+    q = np.asarray(q, np.float64)
+    n2, nq, hd = q.shape
+    n = n2 // 2
+    keys = np.concatenate([k_mem, k_pred], 0).astype(np.float64)
+    vals = np.concatenate([v_mem, v_pred], 0).astype(np.float64)
+    group = nq // keys.shape[1]
+    out = np.zeros((len(rows), nq, hd))
+    for i, r in enumerate(rows):
+        vis = dual_stream_visible_row(n, block, r)
+        for h in range(nq):
+            g = h // group
+            s = (keys[vis, g] @ q[r, h]) / np.sqrt(hd)
+            p = np.exp(s - s.max())
+            out[i, h] = (p / p.sum()) @ vals[vis, g]
     return out
 
 

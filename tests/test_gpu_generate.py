@@ -494,6 +494,40 @@ def test_dual_stream_attention_matches_oracle(n, block):
     ctx.close()
 
 
+def test_dual_stream_attention_at_benchmark_size_sampled_rows():
+    """The benchmark's Dual-Stream call (n = 4096 tokens per stream, blocks of
+    32, 32 q / 8 kv heads of 128), in its own launch configuration: sampled
+    memory and prediction rows (both ends of the streams and of blocks, and
+    random ones) at flat 2e-2 against the oracle evaluated on those rows."""
+    from serving_wedlm_step_gb300.binding import WedlmContext
+    n, block = 4096, 32
+    s = qwen3_layers(1).replace(vocab=1024)
+    nq, nkv, hd = s.n_q_heads, s.n_kv_heads, s.head_dim
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4096)
+    q = torch.randn(2 * n, nq, hd, generator=g, device="cuda").to(torch.bfloat16)
+    kv = [torch.randn(n, nkv, hd, generator=g, device="cuda").to(torch.bfloat16).float()
+          .cpu().numpy() for _ in range(4)]
+    km, vm, kp, vp = kv
+    pool = dev(_pages_in_order(km, vm), torch.bfloat16)
+    win = dev(np.concatenate([_blocks(km, vm, block), _blocks(kp, vp, block)]), torch.bfloat16)
+    w = make_weights_torch(s, seed=0)
+    # the benchmark's context: 512 workspace rows for the partials
+    ctx = WedlmContext(s, w, window=1, max_batch=512, max_pages_per_seq=4)
+    o = torch.empty(2 * n, nq * hd, dtype=torch.bfloat16, device="cuda")
+    ctx.dual_stream_attention(n, block, q, pool, win, o)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    rng = np.random.default_rng(3)
+    rows = sorted(set([0, 1, 31, 32, 2047, n - 1, n, n + 31, n + 32, n + 2048, 2 * n - 1]
+                      + list(rng.integers(0, 2 * n, 13))))
+    ref = O.dual_stream_attention_rows(q.float().cpu().numpy(), km, vm, kp, vp, block, rows)
+    got = o.float().cpu().numpy().reshape(2 * n, nq, hd)[rows]
+    e, ok = within(got, ref, TOL, name="dual_stream_4096")
+    assert ok, e
+    ctx.close()
+
+
 def test_dual_stream_attention_rejects_beyond_workspace():
     from serving_wedlm_step_gb300 import binding as Bd
     s = qwen3_layers(1).replace(vocab=1024)

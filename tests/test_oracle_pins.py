@@ -642,3 +642,17 @@ def test_dual_stream_visibility_counts():
     # no prediction row sees a memory token at or after its block's start
     for i in range(n):
         assert not vis[n + i, (i // block) * block:n].any()
+
+
+def test_dual_stream_rows_equal_the_whole_call():
+    """The row-restricted Dual-Stream attention (used to check sampled rows
+    of large calls) is the whole call's rows: memory rows, prediction rows at
+    every position of a block, both ends."""
+    rng = np.random.default_rng(7)
+    n, block, nq, nkv, hd = 24, 8, 4, 2, 16
+    q = rng.standard_normal((2 * n, nq, hd))
+    km, vm, kp, vp = (rng.standard_normal((n, nkv, hd)) for _ in range(4))
+    full = O.dual_stream_attention(q, km, vm, kp, vp, block)
+    rows = [0, 5, n - 1, n, n + 3, n + 7, n + 8, 2 * n - 1]
+    part = O.dual_stream_attention_rows(q, km, vm, kp, vp, block, rows)
+    assert np.allclose(part, full[rows], rtol=1e-12, atol=1e-12)
