@@ -852,24 +852,29 @@ std::unique_ptr<TcPlanSet> make_tc_plans(const wedlm_config& g,
 
 // split-K factor for the persistent kernel: units = tiles * s are dealt
 // round-robin to num_sms blocks.  Modelled time: the weight stream is bound
-// by the busiest block (about 65 GB/s for one SM streaming one-box weight
-// tiles with its activation blocks) or by the whole GPU (about 6.5 TB/s),
-// whichever is slower; split-K adds a second launch (about 3 us) and the
-// fp32 partial round trip (s * M * N * 8 bytes at about 2 TB/s effective).
-// At least 4 k-blocks per unit.
+// by the busiest block (one SM streaming one-box weight tiles with its
+// activation blocks) or by the whole GPU (about 6.5 TB/s), whichever is
+// slower; split-K adds a second launch (about 3 us) and the fp32 partial
+// round trip (s * M * N * 8 bytes).  The per-SM and partial rates are fitted
+// to forced-plan sweeps on GB300 at the Qwen3-8B shapes: with one 128-row
+// activation block about 100 GB/s per SM and 4 TB/s for the partials (down
+// fastest at 6 splits, O at 5), with more blocks about 65 GB/s and 2 TB/s
+// (the rates that also keep 129..256 rows on the pair kernel, which measured
+// faster there).  At least 4 k-blocks per unit.
 int tc_choose_splits(int tiles, int nkb, int M, int N, int ntile, int num_sms,
                      size_t part_elems, double* time_out) {
   const double w_kb = (double)ntile * kBK * 2, x_kb = (double)((M + 127) / 128) * kXBlockBytes;
   const double t_all = (double)tiles * nkb * w_kb / 6.5e12;
+  const double sm_rate = M <= 128 ? 100e9 : 65e9, part_rate = M <= 128 ? 4e12 : 2e12;
   int best = 1;
   double best_t = 1e30;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && (nkb / s < 4 || (size_t)s * M * N > part_elems)) break;
     const int rounds = (tiles * s + num_sms - 1) / num_sms;
     const int kper = (nkb + s - 1) / s;
-    const double t_sm = (double)rounds * kper * (w_kb + x_kb) / 65e9;
+    const double t_sm = (double)rounds * kper * (w_kb + x_kb) / sm_rate;
     double t = std::max(t_sm, t_all);
-    if (s > 1) t += 3e-6 + (double)s * M * N * 8.0 / 2e12;
+    if (s > 1) t += 3e-6 + (double)s * M * N * 8.0 / part_rate;
     if (t < best_t * (1.0 - 1e-9)) { best_t = t; best = s; }
   }
   if (time_out) *time_out = best_t;
