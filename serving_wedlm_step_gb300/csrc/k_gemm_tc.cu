@@ -105,6 +105,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
   const int nrb_live = (m_live + 127) / 128;
   const uint32_t stage_live = (uint32_t)nrb_live * kXBlockBytes + (uint32_t)ntile * 128u;
+  // the live blocks' accumulators take two buffers whenever two fit in the
+  // TMEM allocation, so that the epilogue of one tile overlaps the MMAs of
+  // the next (the LM head planned for 256 rows with at most 128 of them
+  // masked); with every block live this is the plan's own layout
+  const uint32_t buf_cols = (uint32_t)nrb_live * (uint32_t)ntile;
+  const int nbuf = buf_cols * 2u <= L.tmem_cols ? 2 : 1;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -188,10 +194,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         const int split = u % P.splits;
         const int kb0 = (int)((long long)nkb * split / P.splits);
         const int kb1 = (int)((long long)nkb * (split + 1) / P.splits);
-        const int buf = ul % L.nbuf, use = ul / L.nbuf;
+        const int buf = ul % nbuf, use = ul / nbuf;
         if (!wait_or_abort(&acc_empty[buf], ((uint32_t)use & 1u) ^ 1u, P.err, &s_abort)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)buf * L.buf_cols;
+        const uint32_t d0 = tmem + (uint32_t)buf * buf_cols;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           if (!wait_or_abort(&bar_full[s], ph, P.err, &s_abort)) { alive = false; break; }
           tc_fence_after();
@@ -220,7 +226,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
     int ul = 0;
     for (int u = blockIdx.x; u < units && nrb_live > 0; u += gridDim.x, ++ul) {
       const int tile = u / P.splits, split = u % P.splits;
-      const int buf = ul % L.nbuf, use = ul / L.nbuf;
+      const int buf = ul % nbuf, use = ul / nbuf;
       // on a timeout keep going without waiting (outputs are then invalid and
       // the error word says so): the epilogue warps must stay in step at
       // their named barrier
@@ -228,7 +234,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       tc_fence_after();
       for (int r = 0; r < nrb_live; ++r) {
         const int m = r * 128 + 32 * q + lane;
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols +
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * buf_cols +
                                (uint32_t)(r * ntile);
         if (P.splits == 1) {
           AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < m_live};
