@@ -341,10 +341,11 @@ int wedlm_lm_head(wedlm_ctx *ctx, int32_t batch, const void *x,
  *    WEDLM_ERR_INVALID_ARG.
  *  - Every call shares the array and it keeps the last call's contents:
  *    calls that overlap on the GPU (other streams, other threads) race.
- *  - Nothing found on the device is reported: page ids outside
+ *  - Nothing found on the device makes the call fail: page ids outside
  *    [0, num_pages) read as zeros, and a bounded wait that expires (2 s)
- *    leaves the output partly written; the error word that records either
- *    lives in the array and no call reads it back.
+ *    leaves the output partly written.  Both set bits of an error word in
+ *    the array, cleared at the start of every call and read back by
+ *    wedlm_attention_static_status.
  *  - q, kv_pool, kv_win and o must be 16-byte aligned; n_q_heads a positive
  *    multiple of n_kv_heads.
  *  - Calls no cudaMalloc, cudaFree or allocating library routine. */
@@ -353,6 +354,16 @@ int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q_heads,
                            int32_t num_pages, const void *q, const void *kv_pool,
                            const int32_t *page_table, const int32_t *seq_len,
                            const void *kv_win, void *o, void *stream);
+
+/* The device error word of the last wedlm_attention_static call on the
+ * current device: WEDLM_DEV_* bits (WEDLM_DEV_BAD_PAGE for a page id outside
+ * [0, num_pages), WEDLM_DEV_TIMEOUT for a bounded wait that expired), 0 when
+ * the call found nothing or no call has run on this device.  Waits for
+ * `stream` (the stream the call was issued on) and copies 4 bytes to the
+ * host; allocates nothing.  device_error: host pointer, written on success.
+ * Returns WEDLM_ERR_INVALID_ARG for a null pointer, WEDLM_ERR_CUDA if the
+ * copy or the wait fails. */
+int wedlm_attention_static_status(void *stream, int32_t *device_error);
 
 #ifdef __cplusplus
 }

@@ -27,6 +27,7 @@ EXPORTED = ["wedlm_create", "wedlm_destroy", "wedlm_last_error", "wedlm_get_stat
             "wedlm_set_graphs", "wedlm_set_timing", "wedlm_get_timings",
             "wedlm_launches_per_step", "wedlm_step", "wedlm_reorder_embed",
             "wedlm_layer", "wedlm_attention", "wedlm_lm_head", "wedlm_attention_static",
+            "wedlm_attention_static_status",
             "wedlm_prefill", "wedlm_generate", "wedlm_dual_stream_attention"]
 
 
@@ -101,6 +102,7 @@ def load_library(path: str = LIB_PATH):
     lib.wedlm_lm_head.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_float,
                                   c_void_p, c_void_p, c_void_p]
     lib.wedlm_attention_static.argtypes = [c_int32] * 6 + [c_void_p] * 7
+    lib.wedlm_attention_static_status.argtypes = [c_void_p, POINTER(c_int32)]
     lib.wedlm_prefill.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                   c_int32, POINTER(c_void_p), c_void_p, c_void_p]
     lib.wedlm_generate.argtypes = [c_void_p, POINTER(GenIn), c_void_p]
@@ -345,6 +347,16 @@ def attention_static(window, n_q_heads, n_kv_heads, max_pages_per_seq, num_pages
         _stream_handle(stream))
     if rc != OK:
         raise WedlmError(rc, "wedlm_attention_static failed")
+
+
+def attention_static_status(stream=None):
+    """wedlm_attention_static_status: the WEDLM_DEV_* bits the last
+    attention_static call on the current device set (waits for the stream)."""
+    word = c_int32(0)
+    rc = lib().wedlm_attention_static_status(_stream_handle(stream), ctypes.byref(word))
+    if rc != OK:
+        raise WedlmError(rc, "wedlm_attention_static_status failed")
+    return int(word.value)
 
 
 def rows_to_numpy(rows_tensor):

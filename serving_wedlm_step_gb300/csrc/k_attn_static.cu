@@ -103,3 +103,24 @@ extern "C" int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q
   if (launch_attention_tc(A, scratch + kZeroOff, sms, st) != cudaSuccess) return WEDLM_ERR_CUDA;
   return WEDLM_OK;
 }
+
+extern "C" int wedlm_attention_static_status(void* stream, int32_t* device_error) {
+  if (!device_error) return WEDLM_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WEDLM_ERR_CUDA;
+  uint8_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    scratch = g_addr[dev];
+  }
+  int32_t word = 0;
+  if (scratch) {  // else no call has run on this device
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, scratch + kErrOff, sizeof(word), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return WEDLM_ERR_CUDA;
+  }
+  *device_error = word;
+  return WEDLM_OK;
+}

@@ -42,6 +42,7 @@ def test_attention_static_matches_wedlm_attention_twice():
                             q, pool, pt, sl, win, o_st)
         torch.cuda.synchronize()
         assert ctx.status() == 0
+        assert Bd.attention_static_status() == 0
         outs_ref.append(o_ref.float().cpu().numpy())
         outs_static.append(o_st.float().cpu().numpy())
     for a, b in zip(outs_ref, outs_static):
@@ -49,6 +50,43 @@ def test_attention_static_matches_wedlm_attention_twice():
         assert np.array_equal(a, b), float(np.abs(a - b).max())
     # the two calls really computed different things
     assert np.abs(outs_static[0] - outs_static[1]).max() > 0.1
+    ctx.close()
+
+
+def test_attention_static_status_reports_bad_page_ids():
+    """A page id outside [0, num_pages) reads as zeros and sets
+    WEDLM_DEV_BAD_PAGE in the static array's error word, which the status
+    call reads back; the next clean call clears it and matches
+    wedlm_attention bit for bit."""
+    from serving_wedlm_step_gb300 import binding as Bd
+    from tests.gpu_common import dev
+    s = qwen3_layers(1)
+    B, W = 4, 16
+    wl = Workload("t", s, batch=B, window=W, prefix=(200, 900), masked=(4, 12),
+                  shuffled_pages=True, seed=23)
+    st = make_state_np(wl)
+    pool = make_pool_torch(s, st["num_pages"], 23, 0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    w = make_weights_torch(s, seed=23)
+    ctx = Bd.WedlmContext(s, w, window=W, max_batch=B, max_pages_per_seq=st["max_pages"])
+    q = torch.randn(B * W, s.n_q_heads, s.head_dim, generator=g, device="cuda").to(torch.bfloat16)
+    win = (torch.randn(B, 2, s.n_kv_heads, 16 * s.head_dim, generator=g, device="cuda")
+           .to(torch.bfloat16))
+    bad_pt = st["page_table"].copy()
+    bad_pt[1, 0] = st["num_pages"] + 5
+    o = torch.empty(B * W, s.n_q_heads * s.head_dim, dtype=torch.bfloat16, device="cuda")
+    Bd.attention_static(W, s.n_q_heads, s.n_kv_heads, st["max_pages"], st["num_pages"],
+                        q, pool, dev(bad_pt), dev(st["seq_len"]), win, o)
+    assert Bd.attention_static_status() & Bd.DEV_BAD_PAGE
+    pt, sl = dev(st["page_table"]), dev(st["seq_len"])
+    o_ref = torch.empty_like(o)
+    ctx.attention(q, pool, pt, sl, st["num_pages"], win, o_ref)
+    Bd.attention_static(W, s.n_q_heads, s.n_kv_heads, st["max_pages"], st["num_pages"],
+                        q, pool, pt, sl, win, o)
+    assert Bd.attention_static_status() == 0
+    assert ctx.status() == 0
+    assert torch.equal(o, o_ref)
     ctx.close()
 
 
