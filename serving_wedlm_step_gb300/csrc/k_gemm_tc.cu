@@ -75,9 +75,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   const int nkb = P.K / kBK;
   const int ntile = L.ntile;
   const int units = L.tiles * P.splits;
+  // activation rows present (the LM head on masked rows reads their count,
+  // written at the start of the step); row blocks beyond them are skipped
+  const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
+  const int nrb_live = (m_live + 127) / 128;
+  // with fewer live row blocks than planned, the ring is cut into stages of
+  // the live size, so that more K blocks are in flight; with every block
+  // live this is the plan's own ring
+  const uint32_t a_bytes =
+      nrb_live < L.nrb ? (uint32_t)max(nrb_live, 1) * kXBlockBytes : L.a_bytes;
+  const uint32_t stage_bytes = a_bytes + (uint32_t)ntile * 128u;
+  const int stages = min(kMaxStages, (int)(((uint32_t)L.stages * L.stage_bytes) / stage_bytes));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L.stages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
@@ -100,10 +111,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  // activation rows present (the LM head on masked rows reads their count,
-  // written at the start of the step); row blocks beyond them are skipped
-  const int m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
-  const int nrb_live = (m_live + 127) / 128;
   const uint32_t stage_live = (uint32_t)nrb_live * kXBlockBytes + (uint32_t)ntile * 128u;
   // the live blocks' accumulators take two buffers whenever two fit in the
   // TMEM allocation, so that the epilogue of one tile overlaps the MMAs of
@@ -126,7 +133,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       bool waited = false;
       int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
       auto issue_x = [&](int s, int kx) {
-        uint8_t* st = base + (size_t)s * L.stage_bytes;
+        uint8_t* st = base + (size_t)s * stage_bytes;
         for (int r = 0; r < nrb_live; ++r)
           tma_load_2d(st + r * kXBlockBytes, &mX, &bar_full[s], kx, r * 128);
       };
@@ -150,28 +157,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = ps;
           const uint32_t ph = pph;
-          if (++ps == L.stages) {  // the ring position of the next K block
+          if (++ps == stages) {  // the ring position of the next K block
             ps = 0;
             pph ^= 1u;
           }
           if (!wait_or_abort(&bar_empty[s], ph ^ 1u, P.err, &s_abort)) { alive = false; break; }
-          uint8_t* st = base + (size_t)s * L.stage_bytes;
+          uint8_t* st = base + (size_t)s * stage_bytes;
           mbar_arrive_expect_tx(&bar_full[s], stage_live);
           const int kx = kb * kBK;
           // the weight tile in one box (SwiGLU: gate rows, then up rows);
           // rows of 128 bytes one after another, as the MMA descriptors expect
           if (P.swiglu) {
-            tma_load_2d_hint(st + L.a_bytes, &mW0, &bar_full[s], kx, tile * half, pol);
-            tma_load_2d_hint(st + L.a_bytes + half * 128, &mW1, &bar_full[s], kx, tile * half, pol);
+            tma_load_2d_hint(st + a_bytes, &mW0, &bar_full[s], kx, tile * half, pol);
+            tma_load_2d_hint(st + a_bytes + half * 128, &mW1, &bar_full[s], kx, tile * half, pol);
           } else {
-            tma_load_2d_hint(st + L.a_bytes, seg, &bar_full[s], kx, row0, pol);
+            tma_load_2d_hint(st + a_bytes, seg, &bar_full[s], kx, row0, pol);
           }
           if (waited) {
             issue_x(s, kx);
           } else {
             pend_s[npend] = s;
             pend_kx[npend] = kx;
-            if (++npend == L.stages) wait_prev();
+            if (++npend == stages) wait_prev();
           }
         }
       }
@@ -185,7 +192,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
       // as in the pair kernel: stage and phase stepped, descriptors formed
       // once per stage and stepped along K (2 = 32 bytes in 16-byte units)
       const uint64_t da0 = sdesc_sw128(smem_u32(base));
-      const uint64_t dstage = (uint64_t)(L.stage_bytes >> 4), dw = (uint64_t)(L.a_bytes >> 4);
+      const uint64_t dstage = (uint64_t)(stage_bytes >> 4), dw = (uint64_t)(a_bytes >> 4);
       const uint64_t dx = (uint64_t)(kXBlockBytes >> 4);
       int it = 0, ul = 0, s = 0;
       uint32_t ph = 0;
@@ -210,7 +217,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
                          idesc, (kb != kb0 || kk) ? 1u : 0u);
           }
           tc_commit(&bar_empty[s]);
-          if (++s == L.stages) {
+          if (++s == stages) {
             s = 0;
             ph ^= 1u;
           }
@@ -276,7 +283,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
   if (s_abort && threadIdx.x == 0) {
     // after a timeout: wait (bounded) for this block's copies still in flight
     for (int it = s_consumed; it < s_issued; ++it)
-      mbar_wait(&bar_full[it % L.stages], (uint32_t)(it / L.stages) & 1u, P.err);
+      mbar_wait(&bar_full[it % stages], (uint32_t)(it / stages) & 1u, P.err);
   }
   __syncthreads();
   if (warp == 2) tmem_dealloc(tmem, L.tmem_cols);
