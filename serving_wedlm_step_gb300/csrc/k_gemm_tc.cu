@@ -293,23 +293,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ 
 // order (deterministic), with consecutive threads on consecutive columns so
 // that every partial is read once, coalesced.
 
-// sum of the splits at float4 index i of [M][N]
-// (loads four splits at a time; the additions stay in split order)
+// sum of the splits at float4 index i of [M][N]; the additions stay in
+// split order.  NB > 1: the loads of up to NB splits are issued before the
+// first addition, so that they share one L2 round trip; NB = 1: the loads of
+// four splits at a time only when four remain (fewer registers)
+template <int NB = 4>
 __device__ __forceinline__ float4 splitk_sum4(const GemmProblem& P, size_t i) {
   const float4* p4 = reinterpret_cast<const float4*>(P.partial) + i;
   const size_t stride4 = (size_t)P.M * P.N / 4;
   float4 a = __ldcg(p4);
-  int sp = 1;
-  for (; sp + 3 < P.splits; sp += 4) {
-    float4 t[4];
+  if constexpr (NB > 1) {
+    for (int sp = 1; sp < P.splits; sp += NB) {
+      float4 t[NB];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) t[k] = __ldcg(p4 + (sp + k) * stride4);
+      for (int k = 0; k < NB; ++k)
+        if (sp + k < P.splits) t[k] = __ldcg(p4 + (size_t)(sp + k) * stride4);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) { a.x += t[k].x; a.y += t[k].y; a.z += t[k].z; a.w += t[k].w; }
-  }
-  for (; sp < P.splits; ++sp) {
-    const float4 t = __ldcg(p4 + sp * stride4);
-    a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
+      for (int k = 0; k < NB; ++k)
+        if (sp + k < P.splits) { a.x += t[k].x; a.y += t[k].y; a.z += t[k].z; a.w += t[k].w; }
+    }
+  } else {
+    int sp = 1;
+    for (; sp + 3 < P.splits; sp += 4) {
+      float4 t[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) t[k] = __ldcg(p4 + (sp + k) * stride4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { a.x += t[k].x; a.y += t[k].y; a.z += t[k].z; a.w += t[k].w; }
+    }
+    for (; sp < P.splits; ++sp) {
+      const float4 t = __ldcg(p4 + sp * stride4);
+      a.x += t.x; a.y += t.y; a.z += t.z; a.w += t.w;
+    }
   }
   return a;
 }
@@ -336,7 +351,14 @@ __global__ void __launch_bounds__(256) splitk_resid_kernel(GemmProblem P) {
 // the stored bf16 x, with the same per-thread 8-element vectors and the same
 // reduction order as rmsnorm_kernel, so the result is bit-identical to the
 // two separate kernels.
-__global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmProblem P) {
+// NB = 4: the split loads batched, at most 64 registers (two blocks per
+// SM); NB = 1: fewer loads in flight (about 40 registers, three blocks per
+// SM), for more rows than two blocks per SM hold: measured on GB300, the
+// batched kernel saves 1-2 us per launch at 256 rows, but at 512 rows its
+// second wave of blocks costs the step more than that
+template <int NB>
+__global__ void __launch_bounds__(kNormThreads, NB > 1 ? 2 : 3)
+    splitk_resid_norm_kernel(GemmProblem P) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   const int m = blockIdx.x;
@@ -344,8 +366,8 @@ __global__ void __launch_bounds__(kNormThreads) splitk_resid_norm_kernel(GemmPro
   bf16* x = static_cast<bf16*>(P.epi.x) + (size_t)m * P.N;
   float ss = 0.f;
   for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-    const float4 a0 = splitk_sum4(P, ((size_t)m * P.N) / 4 + 2 * i);
-    const float4 a1 = splitk_sum4(P, ((size_t)m * P.N) / 4 + 2 * i + 1);
+    const float4 a0 = splitk_sum4<NB>(P, ((size_t)m * P.N) / 4 + 2 * i);
+    const float4 a1 = splitk_sum4<NB>(P, ((size_t)m * P.N) / 4 + 2 * i + 1);
     const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
     Vec16<bf16> v = ld16(x + 8 * i);
 #pragma unroll
@@ -411,7 +433,8 @@ __global__ void __launch_bounds__(256) splitk_swiglu_kernel(GemmProblem P, int n
 // q and k heads: per-head RMSNorm (when enabled), then RoPE on the pairs
 // (d, d + 64), which sit in lanes l and l ^ 16; q goes to q_out, k and v
 // to the layer's window scratch in the 8x8-tile layout.
-__global__ void __launch_bounds__(256) splitk_qkv_kernel(GemmProblem P) {
+// (at most 64 registers: four blocks per SM)
+__global__ void __launch_bounds__(256, 4) splitk_qkv_kernel(GemmProblem P) {
   pdl_wait();  // the previous kernel's results
   pdl_trigger();
   const GemmEpi& e = P.epi;
@@ -1194,7 +1217,9 @@ cudaError_t launch_gemm_epilogue(const TcPlanSet& plans, const GemmProblem& P, c
   if (P.splits > 1) {
     const int cap = plans.num_sms * 8;  // grid-stride beyond 8 blocks per SM
     if (norm) {
-      return launch_pdl(splitk_resid_norm_kernel, dim3(P.M), dim3(kNormThreads), 0, st, P);
+      if (P.M > 2 * plans.num_sms)
+        return launch_pdl(splitk_resid_norm_kernel<1>, dim3(P.M), dim3(kNormThreads), 0, st, P);
+      return launch_pdl(splitk_resid_norm_kernel<4>, dim3(P.M), dim3(kNormThreads), 0, st, P);
     } else if (P.epi.mode == EPI_RESID) {
       const size_t n4 = (size_t)P.M * P.N / 4;
       return launch_pdl(splitk_resid_kernel, dim3((int)std::min<size_t>((n4 + 255) / 256, cap)),
