@@ -444,25 +444,36 @@ __global__ void __launch_bounds__(256, 4) splitk_qkv_kernel(GemmProblem P) {
   if (wid >= P.M * heads) return;
   const int m = wid / heads, gh = wid % heads;
   const int kind = gh < e.nq ? 0 : (gh < e.nq + e.nkv ? 1 : 2);
-  const float4 a = splitk_sum4(P, ((size_t)m * P.N + (size_t)gh * 128) / 4 + lane);
-  float x[4] = {a.x, a.y, a.z, a.w};
   const int d0 = 4 * lane;
+  // the norm weights and the RoPE table go out with the partials' loads
+  // (none depends on the sum), not one L2 round trip after them
+  float gw[4] = {1.f, 1.f, 1.f, 1.f}, cs[4] = {}, sn[4] = {};
+  if (kind < 2) {
+    if (e.qk_norm) {
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(
+          static_cast<const bf16*>(kind == 0 ? e.q_norm : e.k_norm) + d0);
+      const float2 g01 = __bfloat1622float2(g2[0]), g23 = __bfloat1622float2(g2[1]);
+      gw[0] = g01.x; gw[1] = g01.y; gw[2] = g23.x; gw[3] = g23.y;
+    }
+    const int dh = d0 & 63;  // position within the rotated half
+    const float4 c4 = *reinterpret_cast<const float4*>(e.cosb + (size_t)m * 64 + dh);
+    const float4 s4 = *reinterpret_cast<const float4*>(e.sinb + (size_t)m * 64 + dh);
+    cs[0] = c4.x; cs[1] = c4.y; cs[2] = c4.z; cs[3] = c4.w;
+    sn[0] = s4.x; sn[1] = s4.y; sn[2] = s4.z; sn[3] = s4.w;
+  }
+  const float4 a = splitk_sum4<3>(P, ((size_t)m * P.N + (size_t)gh * 128) / 4 + lane);
+  float x[4] = {a.x, a.y, a.z, a.w};
   if (kind < 2) {
     if (e.qk_norm) {
       float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
       ss = warp_sum(ss);
       const float rs = rsqrtf(ss / 128.f + e.eps);
-      const bf16* gw = static_cast<const bf16*>(kind == 0 ? e.q_norm : e.k_norm) + d0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) x[k] = x[k] * rs * __bfloat162float(gw[k]);
+      for (int k = 0; k < 4; ++k) x[k] = x[k] * rs * gw[k];
     }
     float y[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) y[k] = __shfl_xor_sync(0xffffffffu, x[k], 16);
-    const int dh = d0 & 63;  // position within the rotated half
-    const float4 c4 = *reinterpret_cast<const float4*>(e.cosb + (size_t)m * 64 + dh);
-    const float4 s4 = *reinterpret_cast<const float4*>(e.sinb + (size_t)m * 64 + dh);
-    const float cs[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
     if (lane < 16) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) x[k] = x[k] * cs[k] - y[k] * sn[k];

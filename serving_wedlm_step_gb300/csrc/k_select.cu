@@ -45,7 +45,17 @@ __global__ void lmhead_merge_kernel(int M, int tiles,
   if (warp >= M || (m_count && warp >= *m_count)) return;
   SoftmaxPart acc;
   acc.m = -INFINITY; acc.a = INT32_MAX; acc.s = 0.f; acc.u = 0.f;
-  for (int t = lane; t < tiles; t += 32) combine(acc, part[(size_t)t * M + warp]);
+  // this lane's records in tile order; the loads of eight go out before
+  // they are combined (one L2 round trip per eight, the order unchanged)
+  for (int t0 = lane; t0 < tiles; t0 += 8 * 32) {
+    SoftmaxPart r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t0 + 32 * k < tiles) r[k] = part[(size_t)(t0 + 32 * k) * M + warp];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t0 + 32 * k < tiles) combine(acc, r[k]);
+  }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     SoftmaxPart b;
