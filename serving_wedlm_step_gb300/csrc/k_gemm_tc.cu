@@ -544,7 +544,7 @@ constexpr int kPairN = 256;                    // widest N of one pair MMA
 // one CTA's half of one MMA's weights per stage: mma_n / 2 rows x 128 bytes
 __host__ __device__ constexpr uint32_t pair_wbytes(int mma_n) { return (uint32_t)mma_n * 64u; }
 
-template <int NMMA>
+template <int NMMA, int NRB = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_constant__ CUtensorMap mW1,
                     const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mX,
@@ -567,6 +567,16 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
   constexpr int nmma = NMMA;
   const int mma_n = L.mma_n, ntile = NMMA * mma_n, hn = mma_n / 2;
   const uint32_t wbytes = pair_wbytes(mma_n);
+  // NRB row blocks of 256 per pair (CTA r holds rows 256 * b + 128 * r of
+  // block b), the weights after them in a stage; with NRB > 1 (the LM head
+  // above 256 rows, masked rows only) the blocks past the live rows are
+  // skipped
+  constexpr uint32_t kABytes = (uint32_t)NRB * kXBlockBytes;
+  int m_live = P.M, nrb_live = 1;
+  if constexpr (NRB > 1) {
+    m_live = P.m_count ? min(P.M, max(0, *P.m_count)) : P.M;
+    nrb_live = max(1, min(NRB, (m_live + 255) / 256));
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
@@ -601,15 +611,19 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
     if (lane == 0) {
       // ---------------- TMA producer (this CTA's halves) ----------------
       const uint64_t pol = l2_evict_first_policy();
-      const uint32_t stage_all = 2u * L.stage_bytes;  // both CTAs
+      // both CTAs
+      const uint32_t stage_all =
+          NRB == 1 ? 2u * L.stage_bytes
+                   : 2u * ((uint32_t)nrb_live * kXBlockBytes + (uint32_t)nmma * wbytes);
       int it = 0, ps = 0;
       uint32_t pph = 0;
       bool alive = true;
       bool waited = false;
       int npend = 0, pend_s[kMaxStages], pend_kx[kMaxStages];
       auto issue_x = [&](int s, int kx) {
-        tma_load_2d_pair_nohint(base + (size_t)s * L.stage_bytes, &mX, full0 + 8u * s, kx,
-                                (int)rank * 128);
+        for (int b = 0; b < nrb_live; ++b)
+          tma_load_2d_pair_nohint(base + (size_t)s * L.stage_bytes + b * kXBlockBytes, &mX,
+                                  full0 + 8u * s, kx, 256 * b + (int)rank * 128);
       };
       auto wait_prev = [&]() {
         pdl_wait();
@@ -659,7 +673,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
           if (rank == 0) mbar_arrive_expect_tx(&bar_full[s], stage_all);
           const int kx = kb * kBK;
           for (int j = 0; j < nmma; ++j)
-            tma_load_2d_pair(st + kXBlockBytes + j * wbytes, segj[j], full0 + 8u * s, kx,
+            tma_load_2d_pair(st + kABytes + j * wbytes, segj[j], full0 + 8u * s, kx,
                              rowj[j], pol);
           if (waited) {
             issue_x(s, kx);
@@ -688,6 +702,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
       const uint64_t da0 = sdesc_sw128(smem_u32(base));
       const uint64_t dstage = (uint64_t)(L.stage_bytes >> 4);
       const uint64_t dw = (uint64_t)(wbytes >> 4), dx = (uint64_t)(kXBlockBytes >> 4);
+      [[maybe_unused]] const uint64_t da_w = (uint64_t)(kABytes >> 4);  // weights after the blocks
       int it = 0, ul = 0, s = 0;
       uint32_t ph = 0;
       bool alive = true;
@@ -706,10 +721,19 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
-            for (int j = 0; j < nmma; ++j)
-              tc_mma_pair_f16(d0 + (uint32_t)(j * mma_n), da + (uint64_t)(2 * kk),
-                              da + dx + (uint64_t)j * dw + (uint64_t)(2 * kk), idesc,
-                              (kb != kb0 || kk) ? 1u : 0u);
+            for (int j = 0; j < nmma; ++j) {
+              if constexpr (NRB == 1) {
+                tc_mma_pair_f16(d0 + (uint32_t)(j * mma_n), da + (uint64_t)(2 * kk),
+                                da + dx + (uint64_t)j * dw + (uint64_t)(2 * kk), idesc,
+                                (kb != kb0 || kk) ? 1u : 0u);
+              } else {
+                for (int b = 0; b < nrb_live; ++b)
+                  tc_mma_pair_f16(d0 + (uint32_t)(b * ntile + j * mma_n),
+                                  da + (uint64_t)b * dx + (uint64_t)(2 * kk),
+                                  da + da_w + (uint64_t)j * dw + (uint64_t)(2 * kk), idesc,
+                                  (kb != kb0 || kk) ? 1u : 0u);
+              }
+            }
           tc_commit_pair(&bar_empty[s], 3);
           if (++s == L.stages) {
             s = 0;
@@ -733,7 +757,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
       const int r = (int)rank;
       const int m = r * 128 + 32 * q + lane;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols;
-      if (P.splits == 1) {
+      if constexpr (NRB > 1) {
+        // no split-K here: each live row block's rows straight from TMEM
+        for (int b = 0; b < nrb_live; ++b) {
+          const int mb = 256 * b + m;
+          AccRow a{ACC_TMEM, taddr + (uint32_t)(b * ntile), nullptr, 0, 1, tile * ntile, P.N,
+                   mb < m_live};
+          tc_epilogue_rows(P, a, mb, tile, ntile, 0, tc_epi_items(P, ntile));
+        }
+      } else if (P.splits == 1) {
         AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
         tc_epilogue_rows(P, a, m, tile, ntile, 0, tc_epi_items(P, ntile));
       } else if (r * 128 + 32 * q < P.M) {
@@ -1067,15 +1099,16 @@ int pair_capacity(size_t smem, int num_sms) {
 }
 
 // dynamic shared memory of a pair launch
-size_t pair_smem(int nmma, int mma_n, int splits) {
-  const uint32_t stage = kXBlockBytes + (uint32_t)nmma * pair_wbytes(mma_n);
+size_t pair_smem(int nmma, int mma_n, int splits, int nrb = 1) {
+  const uint32_t stage = (uint32_t)nrb * kXBlockBytes + (uint32_t)nmma * pair_wbytes(mma_n);
   const uint32_t stg = splits > 1 ? 4 * kStageBoxBytes : 0;
   const uint32_t stages = std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg) / stage);
   return (size_t)stages * stage + stg + 1024;
 }
 
 cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPlan& pp,
-                             int npairs_max, cudaStream_t st, int* tiles_out, int* launches_out) {
+                             int npairs_max, cudaStream_t st, int* tiles_out, int* launches_out,
+                             int nrb = 1) {
   const int ntile = pp.ntile, splits = pp.splits, mma_n = pp.mma_n, nmma = ntile / mma_n;
   const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
   const int bslot = box_slot(mma_n / 2);
@@ -1087,16 +1120,17 @@ cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPl
   const CUtensorMap* a1 = find(P.A1);
   const CUtensorMap* a2 = find(P.A2);
   if (bslot < 0 || !a0 || !a1 || !a2) return cudaErrorInvalidValue;
+  if (nrb != 1 && (nrb != 2 || nmma != 1 || splits != 1)) return cudaErrorInvalidValue;
   TcLaunch L{};
   L.ntile = ntile;
   L.mma_n = mma_n;
-  L.nrb = 1;                                   // one 128-row block per CTA
-  L.buf_cols = ntile;
-  L.nbuf = nmma == 1 ? 2 : 1;                  // 512 TMEM columns either way
+  L.nrb = nrb;                                 // 128-row blocks per CTA
+  L.buf_cols = nrb * ntile;
+  L.nbuf = nmma == 1 && nrb == 1 ? 2 : 1;      // 512 TMEM columns either way
   L.tmem_cols = 512;
-  L.a_bytes = kXBlockBytes;
+  L.a_bytes = (uint32_t)nrb * kXBlockBytes;
   // 32, 40 or 48 KB: multiples of 1024, as the 128-byte swizzle wants
-  L.stage_bytes = kXBlockBytes + nmma * pair_wbytes(mma_n);
+  L.stage_bytes = L.a_bytes + nmma * pair_wbytes(mma_n);
   const uint32_t stg_bytes = splits > 1 ? 4 * kStageBoxBytes : 0;
   L.stages = (int)std::min<uint32_t>(kMaxStages, (kMaxDynSmem - 1024 - stg_bytes) / L.stage_bytes);
   L.stg_off = (uint32_t)L.stages * L.stage_bytes;
@@ -1115,7 +1149,8 @@ cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPl
   const int units = tiles * splits;
   const int npairs = std::min(units, npairs_max);
   const size_t smem = (size_t)L.stages * L.stage_bytes + stg_bytes + 1024;
-  auto kernel = nmma == 1 ? gemm_tc_pair_kernel<1> : gemm_tc_pair_kernel<2>;
+  auto kernel = nrb == 2 ? gemm_tc_pair_kernel<1, 2>
+                         : (nmma == 1 ? gemm_tc_pair_kernel<1> : gemm_tc_pair_kernel<2>);
   cudaError_t e = ensure_dyn_smem((const void*)kernel, kMaxDynSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1142,6 +1177,22 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
                            int* tiles_out, int* launches_out) {
   (void)kind;
   if (P.K % kBK || P.M < 1 || P.M > 512 || P.N % 4) return cudaErrorInvalidValue;
+  // the LM head above 256 rows: SM pairs with two 256-row blocks and
+  // 256-wide vocabulary tiles, so that an SM receives two 16 KB activation
+  // blocks per 16 KB of weights (the one-SM kernel's 128-wide tiles at 512
+  // rows: four per 16 KB)
+  if (P.epi.mode == EPI_LMHEAD && P.M > 256 && !P.swiglu && P.N % 128 == 0) {
+    const int npairs = std::min(plans.num_sms / 2,
+                                pair_capacity(pair_smem(1, kPairN, 1, 2), plans.num_sms));
+    if (npairs > 0) {
+      PairPlan pp;
+      pp.ntile = kPairN;
+      pp.mma_n = kPairN;
+      pp.splits = 1;
+      pp.t = 0.0;
+      return launch_gemm_pair(plans, P, pp, npairs, st, tiles_out, launches_out, 2);
+    }
+  }
   double t_one = 0.0;
   TcChoice choice = tc_plan(plans, P, &t_one);
   if (pair_possible(P)) {
