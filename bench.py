@@ -90,6 +90,16 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def load_tc_sustained():
+    """bf16 tensor peak for kernels timed inside a long step (TFLOP/s)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if "bf16_tflops_sustained" in d:
+            return d["bf16_tflops_sustained"], "measured"
+    return 1700.0, "fallback"
+
+
 # ---------------------------------------------------------------------------
 # algorithmic bytes per launch of each kernel kind (HBM roofline units)
 # ---------------------------------------------------------------------------
@@ -107,6 +117,26 @@ def algorithmic_bytes(shape, B, W, prefix_total):
         "lmhead": es * (V * H + M * H),
         # every cached K/V byte once + window K/V + q in + o out
         "attn": es * (prefix_total * 2 * nkv * hd + B * W * 2 * nkv * hd + 2 * M * nq * hd),
+    }
+
+
+def algorithmic_flops(shape, B, W, prefix_total, masked_rows):
+    """Tensor-core FLOPs per launch of each kind (two per multiply-add): the
+    projections over all B*W rows, the LM head over the masked rows only,
+    the attention over every visible (query row, key) pair, QK^T and P.V
+    (4*hd per pair and q head; a window row at physical p sees its
+    sequence's prefix and window rows 0..p)."""
+    s = shape
+    M = B * W
+    H, hd, nq, nkv, F, V = s.hidden, s.head_dim, s.n_q_heads, s.n_kv_heads, s.ffn, s.vocab
+    pairs = W * prefix_total + B * W * (W + 1) // 2
+    return {
+        "gemm_qkv": 2 * M * H * (nq + 2 * nkv) * hd,
+        "gemm_o": 2 * M * nq * hd * H,
+        "gemm_gateup": 2 * M * H * 2 * F,
+        "gemm_down": 2 * M * F * H,
+        "lmhead": int(2 * masked_rows * V * H),
+        "attn": 4 * nq * hd * pairs,
     }
 
 
@@ -267,18 +297,28 @@ def cpu_sample(wl, w, st, ctx_commits_per_step):
             "seconds_per_step": t_step, "seconds_per_sample": t_sample}
 
 
-def kernel_rates(tim, byts, hbm, n_steps):
+def kernel_rates(tim, byts, hbm, n_steps, flops=None, tc=None):
     """Per-kind CUDA-event times of an eager pass -> launches, us per launch,
-    algorithmic GB/s and fraction of the measured HBM bandwidth."""
+    algorithmic GB/s and fraction of the measured HBM bandwidth, and (with
+    flops and the tensor peak tc in TFLOP/s) algorithmic TFLOP/s, fraction
+    of the tensor peak and which of the two bounds the kind: the larger of
+    bytes / HBM and FLOPs / tensor peak."""
     kernels = {}
     for kind, (kms, n) in tim.items():
         if n == 0:
             continue
         d = {"ms_total": round(kms, 4), "launches": n, "us_per_launch": round(1e3 * kms / n, 2),
              "launches_per_step": round(n / n_steps, 2)}
+        t = kms / n * 1e-3
         if kind in byts:
-            d["gbs"] = round(byts[kind] / (kms / n * 1e-3) / 1e9, 1)
+            d["gbs"] = round(byts[kind] / t / 1e9, 1)
             d["frac_hbm"] = round(d["gbs"] / hbm, 3)
+        if flops and tc and kind in flops:
+            d["tflops"] = round(flops[kind] / t / 1e12, 1)
+            d["frac_tensor"] = round(d["tflops"] / tc, 3)
+            if kind in byts:
+                d["bound"] = ("tensor" if flops[kind] / (tc * 1e12) > byts[kind] / (hbm * 1e9)
+                              else "hbm")
         kernels[kind] = d
     return kernels
 
@@ -398,25 +438,42 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
     torch.cuda.synchronize()
     tim = ctx.timings()
     ctx.set_timing(False)
-    byts = algorithmic_bytes(s, B, W, int(seq_len.sum()) - B * W)  # lengths mid-run
-    hbm, _, peak_src = load_peaks()
-    kernels = kernel_rates(tim, byts, hbm, n_timing)
+    prefix_total = int(seq_len.sum()) - B * W  # lengths mid-run
+    byts = algorithmic_bytes(s, B, W, prefix_total)
+    n_masked = float(np.mean(masked_rows)) if masked_rows else float(B * W)
+    flops = algorithmic_flops(s, B, W, prefix_total, n_masked)
+    hbm, tc, peak_src = load_peaks()
+    tc_sus, _ = load_tc_sustained()
+    kernels = kernel_rates(tim, byts, hbm, n_timing, flops, tc)
     dom = max((k2 for k2 in kernels if k2 in byts), key=lambda k2: kernels[k2]["ms_total"])
     dk = kernels[dom]
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tfile):
         traffic = json.load(open(tfile)).get(f"{name}:{dom}")
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm,
-                "unit": "GB/s", "frac": round(dk["gbs"] / hbm, 3), "traffic": traffic,
-                "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "algorithmic_bytes_per_launch": byts[dom]}
-    # the whole step against the HBM roofline: every kind's algorithmic bytes
-    # times its launches per step, at the measured copy bandwidth
-    step_bytes = sum(byts[k2] * kernels[k2]["launches"] / n_timing for k2 in kernels if k2 in byts)
-    t_roof_ms = step_bytes / (hbm * 1e9) * 1e3
-    step_roofline = {"bound": "hbm", "algorithmic_bytes": int(step_bytes),
+    if dk.get("bound") == "tensor":
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": dk["tflops"], "peak": tc,
+                    "unit": "TFLOP/s", "frac": round(dk["tflops"] / tc, 3), "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)",
+                    "algorithmic_flops_per_launch": flops[dom],
+                    "algorithmic_bytes_per_launch": byts[dom]}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": dk["gbs"], "peak": hbm,
+                    "unit": "GB/s", "frac": round(dk["gbs"] / hbm, 3), "traffic": traffic,
+                    "peak_source": f"{peak_src} hbm_gbs (copy)",
+                    "algorithmic_bytes_per_launch": byts[dom]}
+    # the whole step against its roofline: every kind at the larger of its
+    # algorithmic bytes at the measured copy bandwidth and its FLOPs at the
+    # sustained tensor peak, times its launches per step
+    kind_launches = {k2: kernels[k2]["launches"] / n_timing for k2 in kernels if k2 in byts}
+    step_bytes = sum(byts[k2] * n for k2, n in kind_launches.items())
+    step_flops = sum(flops[k2] * n for k2, n in kind_launches.items())
+    t_roof_ms = sum(max(byts[k2] / (hbm * 1e9), flops[k2] / (tc_sus * 1e12)) * n
+                    for k2, n in kind_launches.items()) * 1e3
+    step_roofline = {"bound": "per kind, the larger of hbm and tensor",
+                     "algorithmic_bytes": int(step_bytes), "algorithmic_flops": int(step_flops),
                      "t_roof_ms": round(t_roof_ms, 4), "peak": hbm, "unit": "GB/s",
+                     "tensor_peak": tc_sus, "tensor_unit": "TFLOP/s (sustained)",
                      "frac": round(t_roof_ms / (ms / steps), 3)}
     launches = ctx.launches_per_step(B)
     # ---- the streaming loop on the device ---------------------------------

@@ -54,3 +54,34 @@ def test_step_bytes_of_the_benchmark_workload():
     # activations (inputs, outputs, residual reads) are ~18 MB a layer
     assert step - (weights + kv) == pytest.approx(s.n_layers * 17.7e6, rel=0.05)
     assert 19e9 < step < 21.5e9
+
+
+def test_flops_per_kind_from_the_shape_and_by_brute_force():
+    """Projections: two FLOPs per weight per row; LM head: over the masked
+    rows only; attention: 4*hd per q head and visible (query, key) pair,
+    counted here pair by pair for a small ragged case."""
+    wl = WORKLOADS["full_stack"]
+    s = wl.shape
+    B, W = 3, 5
+    lens = [7, 0, 19]
+    f = bench.algorithmic_flops(s, B, W, sum(lens), masked_rows=4)
+    M = B * W
+    params = {"gemm_qkv": 4096 * 48 * 128, "gemm_o": 32 * 128 * 4096,
+              "gemm_gateup": 4096 * 2 * 12288, "gemm_down": 12288 * 4096}
+    for kind, p in params.items():
+        assert f[kind] == 2 * M * p, kind
+    assert f["lmhead"] == 2 * 4 * 151936 * 4096
+    pairs = sum(L + p + 1 for L in lens for p in range(W))
+    assert f["attn"] == 4 * 32 * 128 * pairs
+
+
+def test_kernel_bound_is_the_larger_of_hbm_and_tensor_time():
+    # one kind at 1 GB and 1 GFLOP (HBM-bound), one at 1 MB and 1 TFLOP
+    byts = {"a": 10 ** 9, "b": 10 ** 6}
+    flops = {"a": 10 ** 9, "b": 10 ** 12}
+    tim = {"a": (2.0, 2), "b": (4.0, 2)}  # ms total, launches
+    k = bench.kernel_rates(tim, byts, 1000.0, 1, flops, 1000.0)
+    assert k["a"]["bound"] == "hbm" and k["b"]["bound"] == "tensor"
+    assert k["a"]["gbs"] == pytest.approx(1000.0)   # 1 GB in 1 ms
+    assert k["b"]["tflops"] == pytest.approx(500.0)  # 1 TFLOP in 2 ms
+    assert k["b"]["frac_tensor"] == pytest.approx(0.5)
