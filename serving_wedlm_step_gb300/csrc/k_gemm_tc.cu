@@ -758,12 +758,34 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
       const int m = r * 128 + 32 * q + lane;
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)buf * L.buf_cols;
       if constexpr (NRB > 1) {
-        // no split-K here: each live row block's rows straight from TMEM
+        // each live row block's rows straight from TMEM, or their fp32
+        // split-K partials through one staging box per warp (as in
+        // gemm_tc_kernel)
         for (int b = 0; b < nrb_live; ++b) {
           const int mb = 256 * b + m;
-          AccRow a{ACC_TMEM, taddr + (uint32_t)(b * ntile), nullptr, 0, 1, tile * ntile, P.N,
-                   mb < m_live};
-          tc_epilogue_rows(P, a, mb, tile, ntile, 0, tc_epi_items(P, ntile));
+          const uint32_t tb = taddr + (uint32_t)(b * ntile);
+          if (P.splits == 1) {
+            AccRow a{ACC_TMEM, tb, nullptr, 0, 1, tile * ntile, P.N, mb < m_live};
+            tc_epilogue_rows(P, a, mb, tile, ntile, 0, tc_epi_items(P, ntile));
+          } else if (256 * b + r * 128 + 32 * q < m_live) {
+            const uint32_t stg = smem_u32(base + L.stg_off + q * kStageBoxBytes);
+            for (int c = 0; c < ntile && tile * ntile + c < P.N; c += 32) {
+              float v[32];
+              tmem_ld32(tb + (uint32_t)c, v);
+              if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                st_shared_f32x4(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), v[4 * j],
+                                v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&mPart, stg, tile * ntile + c, 256 * b + r * 128 + 32 * q, split);
+                bulk_commit();
+              }
+            }
+          }
         }
       } else if (P.splits == 1) {
         AccRow a{ACC_TMEM, taddr, nullptr, 0, 1, tile * ntile, P.N, m < P.M};
@@ -1035,16 +1057,18 @@ struct PairPlan {
 // the epilogue launch (about 3 us) and the fp32 partials' round trip, which
 // stays in L2 (s * M * N * 8 bytes at about 4 TB/s: measured at 256 rows,
 // QKV is fastest at 3 splits, O and down at 4).
-PairPlan pair_plan(const GemmProblem& P, int nmma, int mma_n, int npairs, size_t part_elems) {
+PairPlan pair_plan(const GemmProblem& P, int nmma, int mma_n, int npairs, size_t part_elems,
+                   int nrb) {
   PairPlan best;
   const int ntile = nmma * mma_n;
   if (npairs < 1 || (P.swiglu ? (P.N / 2) % (ntile / 2) : P.N % 128)) return best;
   if (mma_n != kPairN && !P.swiglu) return best;  // q|k|v segments fall on 128-row halves
+  if (nrb * ntile > 512) return best;             // the accumulators of all row blocks in TMEM
   const int nkb = P.K / kBK;
   const int tiles = P.swiglu ? (P.N / 2) / (ntile / 2) : (P.N + ntile - 1) / ntile;
   const double per_kb = std::max(
-      ((double)kXBlockBytes + nmma * (double)pair_wbytes(mma_n)) / 65e9,
-      nmma * (kBK / 16) * 128.0 * mma_n / kPairN / 1.9e9);
+      ((double)nrb * kXBlockBytes + nmma * (double)pair_wbytes(mma_n)) / 65e9,
+      nrb * nmma * (kBK / 16) * 128.0 * mma_n / kPairN / 1.9e9);
   const double t_all = (double)tiles * nkb * 2.0 * nmma * pair_wbytes(mma_n) / 6.5e12;
   for (int s = 1; s <= 16; ++s) {
     if (s > 1 && (nkb / s < 4 || (size_t)s * P.M * P.N > part_elems)) break;
@@ -1120,7 +1144,7 @@ cudaError_t launch_gemm_pair(const TcPlanSet& plans, GemmProblem P, const PairPl
   const CUtensorMap* a1 = find(P.A1);
   const CUtensorMap* a2 = find(P.A2);
   if (bslot < 0 || !a0 || !a1 || !a2) return cudaErrorInvalidValue;
-  if (nrb != 1 && (nrb != 2 || nmma != 1 || splits != 1)) return cudaErrorInvalidValue;
+  if (nrb != 1 && (nrb != 2 || nmma != 1)) return cudaErrorInvalidValue;
   TcLaunch L{};
   L.ntile = ntile;
   L.mma_n = mma_n;
@@ -1206,11 +1230,22 @@ cudaError_t launch_gemm_tc(const TcPlanSet& plans, GemmProblem P, int kind, cuda
         npairs = std::min(npairs, pair_capacity(pair_smem(sh[0], sh[1], sp), plans.num_sms));
     PairPlan best;
     for (const auto& sh : kShapes) {
-      const PairPlan pp = pair_plan(P, sh[0], sh[1], npairs, plans.part_elems);
+      const PairPlan pp = pair_plan(P, sh[0], sh[1], npairs, plans.part_elems, 1);
       if (pp.t < best.t) best = pp;
     }
     if (best.ntile && best.t < t_one)
       return launch_gemm_pair(plans, P, best, npairs, st, tiles_out, launches_out);
+  }
+  // 257..512 rows: SM pairs with two 256-row blocks (one N = 256 MMA per
+  // block and K step, 512 TMEM columns) when the model prefers them
+  if (P.M > 256 && P.epi.mode != EPI_LMHEAD && !P.m_count &&
+      (P.swiglu ? (P.N / 2) % 128 == 0 : P.N % 128 == 0)) {
+    int npairs = plans.num_sms / 2;
+    for (int sp : {1, 2})
+      npairs = std::min(npairs, pair_capacity(pair_smem(1, kPairN, sp, 2), plans.num_sms));
+    const PairPlan pp = pair_plan(P, 1, kPairN, npairs, plans.part_elems, 2);
+    if (pp.ntile && pp.t < t_one)
+      return launch_gemm_pair(plans, P, pp, npairs, st, tiles_out, launches_out, 2);
   }
   // rows counted on the device (the LM head on masked rows): no split-K, so
   // that no epilogue kernel has to learn the count
