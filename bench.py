@@ -422,9 +422,11 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
             for k2 in host:
                 host[k2].copy_(back[k2])
         e2e_s = time.perf_counter() - t0
+        # committed tokens per step depend on where the sequences are, so the
+        # step time is given too, for a like-for-like latency comparison
         e2e_rec = {"value": round(n_e2e / e2e_s, 2), "unit": "committed tokens/s",
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                   "steps": e2e_steps}
+                   "steps": e2e_steps, "ms_per_step": round(1e3 * e2e_s / e2e_steps, 4)}
         # continue from the state the end-to-end loop left
         for k2 in ("tokens", "pos", "obs"):
             bufs[k % 2][k2].copy_(host[k2].to(device))
