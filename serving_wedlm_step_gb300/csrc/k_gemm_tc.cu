@@ -520,15 +520,16 @@ splitk_epilogue_kernel(GemmProblem P, int ntile, int items) {
 }
 
 // ---------------------------------------------------------------------------
-// 2-SM variant for 129..256 activation rows: a cluster of two CTAs (an SM
-// pair) computes one 256-row x (mma_n * nmma)-feature tile with
+// 2-SM variant for 129..512 activation rows: a cluster of two CTAs (an SM
+// pair) computes one 256-row x (mma_n * nmma)-feature tile (NRB of them
+// over the same weights above 256 rows) with
 // tcgen05.mma.cta_group::2 (nmma MMAs of N = mma_n per K step, one per
 // mma_n-column accumulator; mma_n = 256, or 192 for SwiGLU tiles of 192
 // gate + 192 up features).  CTA r of the pair holds activation rows
 // 128r..128r+127 and, for each MMA, half r of its mma_n weight rows in its
 // shared memory, so each SM receives half the tile's activations and half
-// its weights; its TMEM receives its 128 rows of the tile.  Roles as in
-// gemm_tc_kernel:
+// its weights; its TMEM receives its 128 rows of the tile (rows
+// 256b + 128r.. of each row block b).  Roles as in gemm_tc_kernel:
 //   warp 0 / lane 0 (both CTAs): TMA producer for this CTA's halves; the
 //       loads complete on the even CTA's full barrier (cta_group::2 form),
 //       on which the even CTA's producer set the bytes of both;
@@ -568,9 +569,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mW0, const __grid_consta
   const int mma_n = L.mma_n, ntile = NMMA * mma_n, hn = mma_n / 2;
   const uint32_t wbytes = pair_wbytes(mma_n);
   // NRB row blocks of 256 per pair (CTA r holds rows 256 * b + 128 * r of
-  // block b), the weights after them in a stage; with NRB > 1 (the LM head
-  // above 256 rows, masked rows only) the blocks past the live rows are
-  // skipped
+  // block b), the weights after them in a stage; with NRB > 1 (above 256
+  // rows: the projections, and the LM head on its masked rows) the blocks
+  // past the live rows are skipped
   constexpr uint32_t kABytes = (uint32_t)NRB * kXBlockBytes;
   int m_live = P.M, nrb_live = 1;
   if constexpr (NRB > 1) {
@@ -1032,9 +1033,11 @@ TcChoice tc_plan(const TcPlanSet& plans, const GemmProblem& P, double* t_out) {
 cudaError_t launch_gemm_epilogue(const TcPlanSet& plans, const GemmProblem& P, const TcLaunch& L,
                                  cudaStream_t st);
 
-// The 2-SM pair kernel may take the projections with 129..256 activation
-// rows (two 128-row blocks, one per SM of the pair); the LM head keeps the
-// one-SM kernel (its row count may be known on the device only).
+// The 2-SM pair kernel with one row block may take the projections with
+// 129..256 activation rows (two 128-row halves, one per SM of the pair); at
+// that size the LM head keeps the one-SM kernel (its row count may be known
+// on the device only, and is mostly under 128 there).  Above 256 rows the
+// pair kernel with two row blocks is planned separately.
 bool pair_possible(const GemmProblem& P) {
   if (P.M <= 128 || P.M > 256 || P.epi.mode == EPI_LMHEAD || P.m_count) return false;
   return P.swiglu ? (P.N / 2) % 128 == 0 : P.N % 128 == 0;
@@ -1050,9 +1053,9 @@ struct PairPlan {
 // features, which puts the Qwen3-8B-sized gate/up projection on 64 tiles
 // instead of 48) and its split-K factor: units = tiles * s over the pairs.
 // Modelled time per K block: each SM receives its halves of the activations
-// (16 KB) and of every MMA's weights (mma_n/2 rows x 128 B), at about
+// (16 KB per row block) and of every MMA's weights (mma_n/2 rows x 128 B), at about
 // 65 GB/s per SM as measured on GB300 inside these kernels, or runs its MMAs
-// (128 cycles per M = 256, N = 256, K = 16 pair MMA), whichever is slower;
+// (128 cycles per M = 256, N = 256, K = 16 pair MMA, per row block), whichever is slower;
 // the whole GPU streams the weights at about 6.5 TB/s at most.  Split-K adds
 // the epilogue launch (about 3 us) and the fp32 partials' round trip, which
 // stays in L2 (s * M * N * 8 bytes at about 4 TB/s: measured at 256 rows,
