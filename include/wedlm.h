@@ -365,6 +365,22 @@ int wedlm_attention_static(int32_t batch, int32_t window, int32_t n_q_heads,
  * copy or the wait fails. */
 int wedlm_attention_static_status(void *stream, int32_t *device_error);
 
+/* ---- failure detection self-test ---------------------------------------- */
+
+/* Self-test of the bounded waits every kernel uses (failure detection
+ * without a GPU fault).  One thread waits on a shared-memory barrier that
+ * nothing completes; after the wait limit (2 s) the wait gives up, sets
+ * WEDLM_DEV_TIMEOUT in an error word and the kernel returns, leaving the CUDA
+ * context usable.  Not part of WeDLM; a diagnostic of this library.
+ *  - word: device int32[2], caller-owned, 4-byte aligned; cleared here, then
+ *    word[0] receives the error bits and word[1] 1 if the wait gave up (2 if
+ *    the barrier completed, which nothing makes happen).
+ *  - device_error, gave_up: host pointers, receive word[0] and word[1].
+ * Synchronises `stream` (about 2 s).  Returns WEDLM_ERR_INVALID_ARG for null
+ * or misaligned pointers, WEDLM_ERR_CUDA if the launch, copy or wait fails. */
+int wedlm_selftest_bounded_wait(int32_t *word, int32_t *device_error, int32_t *gave_up,
+                                void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ EXPORTED = ["wedlm_create", "wedlm_destroy", "wedlm_last_error", "wedlm_get_stat
             "wedlm_set_graphs", "wedlm_set_timing", "wedlm_get_timings",
             "wedlm_launches_per_step", "wedlm_step", "wedlm_reorder_embed",
             "wedlm_layer", "wedlm_attention", "wedlm_lm_head", "wedlm_attention_static",
-            "wedlm_attention_static_status",
+            "wedlm_attention_static_status", "wedlm_selftest_bounded_wait",
             "wedlm_prefill", "wedlm_generate", "wedlm_dual_stream_attention"]
 
 
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
                                   c_void_p, c_void_p, c_void_p]
     lib.wedlm_attention_static.argtypes = [c_int32] * 6 + [c_void_p] * 7
     lib.wedlm_attention_static_status.argtypes = [c_void_p, POINTER(c_int32)]
+    lib.wedlm_selftest_bounded_wait.argtypes = [c_void_p, POINTER(c_int32), POINTER(c_int32),
+                                                c_void_p]
     lib.wedlm_prefill.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                   c_int32, POINTER(c_void_p), c_void_p, c_void_p]
     lib.wedlm_generate.argtypes = [c_void_p, POINTER(GenIn), c_void_p]
@@ -347,6 +349,18 @@ def attention_static(window, n_q_heads, n_kv_heads, max_pages_per_seq, num_pages
         _stream_handle(stream))
     if rc != OK:
         raise WedlmError(rc, "wedlm_attention_static failed")
+
+
+def selftest_bounded_wait(word, stream=None):
+    """wedlm_selftest_bounded_wait: a kernel waits on a barrier nothing
+    completes until its bounded wait gives up (about 2 s).  word: device
+    int32 tensor of 2.  Returns (device error bits, 1 if the wait gave up)."""
+    err, gave = c_int32(0), c_int32(0)
+    rc = lib().wedlm_selftest_bounded_wait(_ptr(word), ctypes.byref(err), ctypes.byref(gave),
+                                           _stream_handle(stream))
+    if rc != OK:
+        raise WedlmError(rc, "wedlm_selftest_bounded_wait failed")
+    return int(err.value), int(gave.value)
 
 
 def attention_static_status(stream=None):
