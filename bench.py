@@ -697,8 +697,12 @@ def run_reference(args):
     st = make_state_np(wl)
     # the oracle needs one layer + the LM head: draw them on the CPU
     w = make_weights_torch(s.replace(n_layers=1), seed=wl.seed, device="cpu")
-    # committed tokens per step of the same stream on the GPU arm (measured
-    # there; the oracle's selection rule gives the same counts)
+    # committed tokens per step: one per sequence, the least a step of the
+    # stream commits on average (every step fills at least one slot of each
+    # sequence).  The sample does not run the whole LM head, so it cannot
+    # count the commits; the GPU arm counts its own (several per sequence on
+    # the planted workload, and its cpu_baseline uses that count), so this
+    # rate is a lower bound of the oracle's
     commits_per_step = float(wl.batch)
     samples, sample_s = [], []
     t_all = time.perf_counter()
@@ -716,7 +720,7 @@ def run_reference(args):
            "metric": "committed tokens/s of the window decode step (step latency in ms_per_step)",
            "value": round(value, 6), "unit": "committed tokens/s", "n_gpus": world,
            "steps": len(samples), "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 1),
-           "extrapolated": True,
+           "extrapolated": True, "commits_per_step_assumed": commits_per_step,
            "sample_seconds": round(statistics.median(sample_s), 3) if sample_s else None,
            "note": ("each of the `steps` samples runs one layer of one sequence, two LM-head "
                     "rows and one selection of the oracle; ms_per_step is that sample scaled "
