@@ -333,6 +333,7 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
     Returns (result dict, workload, state, weights, committed tokens per
     step)."""
     import torch
+    from serving_wedlm_step_gb300 import binding as Bd
     from serving_wedlm_step_gb300.binding import WedlmContext
     steps = timed_steps or args.steps
     wl, st, w, pools, plant = setup(name, steps, args.warmup, device, weights, loop_steps)
@@ -395,32 +396,41 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
     if e2e:
         e2e_steps = max(4, min(steps, 32))
         last = bufs[k % 2]
-        host = {k2: last[k2].cpu().pin_memory() for k2 in ("tokens", "pos", "obs")}
-        cur = {k2: v.to(device) for k2, v in host.items()}
-        back = {k2: torch.empty_like(host[k2]).pin_memory() for k2 in ("tokens", "pos", "obs")}
-        back_c = torch.empty(B, W, dtype=torch.int32).pin_memory()
-        back_n = torch.empty(B, dtype=torch.int32).pin_memory()
-        out = ctx.make_outputs(B, device=device)
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(v.numel() * v.element_size() for v in back.values()) + back_c.numel() * 4 + B * 4
+        # the window goes in as one pinned byte buffer (int32 tokens | int32
+        # pos | uint8 observed) and the results come back as one (the packed
+        # step outputs): one copy each way per step
+        n = B * W
+        in_bytes = 8 * n + n
+
+        def window_views(buf):
+            return {"tokens": buf[0:4 * n].view(torch.int32).view(B, W),
+                    "pos": buf[4 * n:8 * n].view(torch.int32).view(B, W),
+                    "obs": buf[8 * n:9 * n].view(B, W)}
+
+        host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        host = window_views(host_in)
+        for k2 in host:
+            host[k2].copy_(last[k2].cpu())
+        dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=device)
+        cur = window_views(dev_in)
+        out = ctx.make_outputs(B, device=device, packed=True)
+        host_out = torch.empty(out["packed"].numel(), dtype=torch.uint8).pin_memory()
+        back = Bd.step_result_views(host_out, B, W)
+        h2d, d2h = in_bytes, host_out.numel()
         n_e2e = 0
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            for k2 in cur:
-                cur[k2].copy_(host[k2], non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
             ctx.step(cur["tokens"], cur["pos"], cur["obs"], seq_len, page_table, pools,
                      st["num_pages"], wl.alpha, wl.tau, out, plant_token=plant_t,
                      plant_bias=bias, stream=stream)
-            back["tokens"].copy_(out["new_tokens"], non_blocking=True)
-            back["pos"].copy_(out["new_pos"], non_blocking=True)
-            back["obs"].copy_(out["new_observed"], non_blocking=True)
-            back_c.copy_(out["committed"], non_blocking=True)
-            back_n.copy_(out["n_committed"], non_blocking=True)
+            host_out.copy_(out["packed"], non_blocking=True)
             stream.synchronize()
-            n_e2e += int(back_n.sum())
-            for k2 in host:
-                host[k2].copy_(back[k2])
+            n_e2e += int(back["n_committed"].sum())
+            host["tokens"].copy_(back["new_tokens"])
+            host["pos"].copy_(back["new_pos"])
+            host["obs"].copy_(back["new_observed"])
         e2e_s = time.perf_counter() - t0
         # committed tokens per step depend on where the sequences are, so the
         # step time is given too, for a like-for-like latency comparison

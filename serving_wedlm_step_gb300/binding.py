@@ -229,17 +229,26 @@ class WedlmContext:
 
     # -- the step ------------------------------------------------------------
     def make_outputs(self, batch, rows=False, logits=False, perm=False, hidden=False,
-                     device="cuda"):
+                     device="cuda", packed=False):
+        """Output tensors of a step.  packed=True places the window and commit
+        results in one byte buffer (out["packed"], the layout of
+        step_result_views), so that a caller reads them back with one copy."""
         import torch
         W = self.window
-        out = {
-            "new_tokens": torch.empty(batch, W, dtype=torch.int32, device=device),
-            "new_pos": torch.empty(batch, W, dtype=torch.int32, device=device),
-            "new_observed": torch.empty(batch, W, dtype=torch.uint8, device=device),
-            "committed": torch.empty(batch, W, dtype=torch.int32, device=device),
-            "n_committed": torch.empty(batch, dtype=torch.int32, device=device),
-            "filled": torch.empty(batch, W, dtype=torch.uint8, device=device),
-        }
+        if packed:
+            buf = torch.empty(step_result_bytes(batch, W), dtype=torch.uint8, device=device)
+            out = step_result_views(buf, batch, W)
+            out["packed"] = buf
+            out["filled"] = torch.empty(batch, W, dtype=torch.uint8, device=device)
+        else:
+            out = {
+                "new_tokens": torch.empty(batch, W, dtype=torch.int32, device=device),
+                "new_pos": torch.empty(batch, W, dtype=torch.int32, device=device),
+                "new_observed": torch.empty(batch, W, dtype=torch.uint8, device=device),
+                "committed": torch.empty(batch, W, dtype=torch.int32, device=device),
+                "n_committed": torch.empty(batch, dtype=torch.int32, device=device),
+                "filled": torch.empty(batch, W, dtype=torch.uint8, device=device),
+            }
         if perm:
             out["perm"] = torch.empty(batch, W, dtype=torch.int32, device=device)
         if rows:
@@ -336,6 +345,33 @@ class WedlmContext:
         self._check(self._lib.wedlm_lm_head(
             self._h, batch, _ptr(x), _ptr(plant_token), plant_bias, _ptr(rows_out),
             _ptr(logits), _stream_handle(stream)))
+
+
+def _aligned(n, a=256):
+    return (n + a - 1) // a * a
+
+
+def step_result_bytes(batch, W):
+    """Bytes of the packed step results: int32 new_tokens, new_pos and
+    committed [B][W], int32 n_committed [B], uint8 new_observed [B][W], each
+    starting on a 256-byte boundary."""
+    n = batch * W
+    return 3 * _aligned(4 * n) + _aligned(4 * batch) + _aligned(n)
+
+
+def step_result_views(buf, batch, W):
+    """Views of a packed step-result byte buffer (device or host) by name."""
+    import torch
+    n = batch * W
+    o, views = 0, {}
+    for name, nbytes, dt, shape in (("new_tokens", 4 * n, torch.int32, (batch, W)),
+                                    ("new_pos", 4 * n, torch.int32, (batch, W)),
+                                    ("committed", 4 * n, torch.int32, (batch, W)),
+                                    ("n_committed", 4 * batch, torch.int32, (batch,)),
+                                    ("new_observed", n, torch.uint8, (batch, W))):
+        views[name] = buf[o:o + nbytes].view(dt).view(*shape)
+        o += _aligned(nbytes)
+    return views
 
 
 def attention_static(window, n_q_heads, n_kv_heads, max_pages_per_seq, num_pages, q, kv_pool,

@@ -233,3 +233,33 @@ def test_host_argument_errors():
         ctx_for(s.replace(head_dim=48), w_np, 8, 1, 4)
     with pytest.raises(B.WedlmError):
         ctx_for(s, w_np, 100, 1, 4)
+
+
+def test_packed_outputs_match_separate_outputs():
+    """make_outputs(packed=True) puts the window and commit results in one
+    byte buffer (one copy back for a caller); the step writes the same
+    values as into separate tensors, and the host-side views of a copy of
+    the buffer read them back."""
+    from serving_wedlm_step_gb300 import binding as B
+    from tests.gpu_common import state_to_dev
+    s, wl, w_np, st, pools_np = make_case(batch=3, seed=41)
+    ctx = ctx_for(s, w_np, wl.window, wl.batch, st["max_pages"])
+    res = []
+    for packed in (False, True):
+        d = state_to_dev(st)
+        pools = [dev(p) for p in pools_np]
+        out = ctx.make_outputs(wl.batch, packed=packed)
+        ctx.step(d["tokens"], d["pos"], d["obs"], d["seq_len"], d["page_table"], pools,
+                 st["num_pages"], 0.01, 1.0, out)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        if packed:
+            host = out["packed"].cpu()
+            views = B.step_result_views(host, wl.batch, wl.window)
+            assert host.numel() == B.step_result_bytes(wl.batch, wl.window)
+        else:
+            views = {k: out[k].cpu() for k in ("new_tokens", "new_pos", "committed",
+                                               "n_committed", "new_observed")}
+        res.append(views)
+    for k in res[0]:
+        assert torch.equal(res[0][k], res[1][k]), k
