@@ -416,6 +416,10 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
         out = ctx.make_outputs(B, device=device, packed=True)
         host_out = torch.empty(out["packed"].numel(), dtype=torch.uint8).pin_memory()
         back = Bd.step_result_views(host_out, B, W)
+        # NumPy views of the pinned buffers: the host side of a step (the
+        # commit count, the next window) without a torch dispatch per op
+        host_np = {k2: v.numpy() for k2, v in host.items()}
+        back_np = {k2: v.numpy() for k2, v in back.items()}
         h2d, d2h = in_bytes, host_out.numel()
         n_e2e = 0
         torch.cuda.synchronize()
@@ -427,10 +431,10 @@ def measure(name, args, device, rank, world, weights=None, timed_steps=None, e2e
                      plant_bias=bias, stream=stream)
             host_out.copy_(out["packed"], non_blocking=True)
             stream.synchronize()
-            n_e2e += int(back["n_committed"].sum())
-            host["tokens"].copy_(back["new_tokens"])
-            host["pos"].copy_(back["new_pos"])
-            host["obs"].copy_(back["new_observed"])
+            n_e2e += int(back_np["n_committed"].sum())
+            host_np["tokens"][...] = back_np["new_tokens"]
+            host_np["pos"][...] = back_np["new_pos"]
+            host_np["obs"][...] = back_np["new_observed"]
         e2e_s = time.perf_counter() - t0
         # committed tokens per step depend on where the sequences are, so the
         # step time is given too, for a like-for-like latency comparison
